@@ -1,0 +1,128 @@
+"""Test infrastructure only: the fp64 CPU oracle for causal NeoX-rotary attention.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path
+(``causal_rope_self_neox_b300``) never does, and shares no code with it.
+
+The arithmetic lives in ``neox_oracle.c`` (plain C, fp64, pthreads); this module
+compiles it with gcc when the shared library is missing and wraps it with ctypes.
+Every function takes the packed ``qkv[B,S,H,3,D]`` bf16 input as its raw 16-bit
+patterns (a ``numpy.uint16`` array), because the oracle widens bf16 to fp64 itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "neox_oracle.c")
+_LIB = os.path.join(_HERE, "libneox_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``neox_oracle.c`` into ``libneox_oracle.so`` (gcc, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+                               "-D_POSIX_C_SOURCE=200809L", _SRC, "-o", tmp, "-lm", "-lpthread"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.neox_oracle_inv_freq.argtypes = [i32, f64, P]
+            lib.neox_oracle_inv_freq.restype = None
+            lib.neox_oracle_rotate.argtypes = [P, i32, i32, f64, i64, P]
+            lib.neox_oracle_rotate.restype = None
+            lib.neox_oracle_fwd.argtypes = [P, i32, i32, i32, i32, i32, f64, P, P, i32]
+            lib.neox_oracle_fwd.restype = i32
+            lib.neox_oracle_fwd_rows.argtypes = [P, i32, i32, i32, i32, i32, f64, P, i64, P, P, i32]
+            lib.neox_oracle_fwd_rows.restype = i32
+            lib.neox_oracle_probs.argtypes = [P, i32, i32, i32, i32, i32, f64, i32, i32, i32, P]
+            lib.neox_oracle_probs.restype = i32
+            _lib = lib
+    return _lib
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1))
+
+
+def _u16(qkv_bits: np.ndarray, shape) -> np.ndarray:
+    a = np.ascontiguousarray(qkv_bits)
+    if a.dtype != np.uint16:
+        raise TypeError("qkv must be passed as bf16 bit patterns (numpy.uint16)")
+    if a.size != int(np.prod(shape)):
+        raise ValueError(f"qkv has {a.size} elements, expected {shape}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def inv_freq(rotary_dim: int, base: float) -> np.ndarray:
+    """inv_freq[i] = base^(-2i/rotary_dim), i < rotary_dim/2 (fp64)."""
+    out = np.zeros(rotary_dim // 2, dtype=np.float64)
+    _load().neox_oracle_inv_freq(rotary_dim, float(base), _ptr(out))
+    return out
+
+
+def rotate(x: np.ndarray, pos: int, rotary_dim: int, base: float) -> np.ndarray:
+    """Rotate-half rotary embedding of one head vector ``x[D]`` (fp64) at position ``pos``."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty_like(x)
+    _load().neox_oracle_rotate(_ptr(x), x.shape[0], rotary_dim, float(base), int(pos), _ptr(y))
+    return y
+
+
+def fwd(qkv_bits: np.ndarray, B: int, S: int, H: int, D: int, rotary_dim: int, base: float,
+        threads: int | None = None):
+    """All rows.  Returns ``(out[B,S,H,D] fp64, lse[B,H,S] fp64)``."""
+    q = _u16(qkv_bits, (B, S, H, 3, D))
+    out = np.empty((B, S, H, D), dtype=np.float64)
+    lse = np.empty((B, H, S), dtype=np.float64)
+    rc = _load().neox_oracle_fwd(_ptr(q), B, S, H, D, rotary_dim, float(base), _ptr(out), _ptr(lse),
+                                 threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"neox_oracle_fwd failed: {rc}")
+    return out, lse
+
+
+def fwd_rows(qkv_bits: np.ndarray, B: int, S: int, H: int, D: int, rotary_dim: int, base: float,
+             rows, threads: int | None = None):
+    """Listed rows ``rows[n,3] = (b, h, i)``.  Returns ``(out[n,D], lse[n])`` in fp64."""
+    q = _u16(qkv_bits, (B, S, H, 3, D))
+    R = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = R.shape[0]
+    out = np.empty((n, D), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    rc = _load().neox_oracle_fwd_rows(_ptr(q), B, S, H, D, rotary_dim, float(base), _ptr(R), n,
+                                      _ptr(out), _ptr(lse), threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"neox_oracle_fwd_rows failed: {rc}")
+    return out, lse
+
+
+def probs(qkv_bits: np.ndarray, B: int, S: int, H: int, D: int, rotary_dim: int, base: float,
+          b: int, h: int, i: int) -> np.ndarray:
+    """The softmax probability row ``p[0..i]`` of query ``(b, h, i)`` (fp64)."""
+    q = _u16(qkv_bits, (B, S, H, 3, D))
+    p = np.empty((i + 1,), dtype=np.float64)
+    rc = _load().neox_oracle_probs(_ptr(q), B, S, H, D, rotary_dim, float(base), b, h, i, _ptr(p))
+    if rc != 0:
+        raise RuntimeError(f"neox_oracle_probs failed: {rc}")
+    return p

@@ -1,0 +1,312 @@
+/*
+ * neox_oracle.c -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, fp64 CPU statement of exact causal multi-head self-attention
+ * with GPT-NeoX rotary position embedding ("Neox style", rotate-half) applied to
+ * the first rotary_dim dims of both Query and Key.  Only the test suite, the
+ * smoke check and the CPU-baseline leg of the benchmark may load this file's
+ * library.  The CUDA path in causal_rope_self_neox_b300/ shares no code with it.
+ *
+ * Where each step comes from (page title, section):
+ *  - exact (not approximated) causal softmax attention, O(n^2) compute:
+ *      "gpt-neox - 模型与框架" (pomoai hub page), section "问题二：注意力计算太慢".
+ *  - rotary embedding on BOTH Query and Key, Neox style, rotary_embedding=24 of
+ *    size_per_head=96 (partial rotary), QK accumulation in fp32 by default,
+ *    fused query_key_value projection whose HuggingFace layout
+ *    [hidden, num_heads, 3, head_hidden] gives a per-token packed [H,3,D]:
+ *      "GPT-NeoX on FasterTransformer" guide, sections "背景", "模型配置（config.ini）"
+ *      and "从 HuggingFace 检查点部署".
+ *  - rotate-half pairing (dim i with dim i+r/2), inv_freq = base^(-2i/r),
+ *    scale 1/sqrt(D), outputs out[B,S,H,D] and the natural-log row
+ *    logsumexp lse[B,H,S]: the problem statement of this op (the pages name
+ *    the stored attention.rotary_emb.inv_freq tensor but print no formula).
+ *
+ * Readings where the pages are silent (each listed in the design notes):
+ *  - positions are 0..S-1 for every sequence, the same for Q and K;
+ *  - the causal mask keeps keys j <= i (diagonal included);
+ *  - the rotation is exact: no rounding of the rotated Q/K anywhere here;
+ *  - no dropout, no bias, no ALiBi.
+ *
+ * Steps are written in the order of the definition, with no tiling, no online
+ * softmax and no fusion:  widen bf16 -> fp64;  inv_freq;  rotate q_s and k_s by
+ * angle s*inv_freq;  scores q'_i.k'_j / sqrt(D) for j <= i;  max;  exp;  sum;
+ * weighted sum of v_j;  lse = max + ln(sum).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ERR_ARG (-1)
+#define ORACLE_ERR_NOMEM (-2)
+
+/* bf16 -> fp64: a bf16 value is the top 16 bits of an IEEE fp32; widening is exact. */
+static double bf16_to_f64(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* inv_freq[i] = base^(-2i / r), i = 0 .. r/2-1. */
+void neox_oracle_inv_freq(int r, double base, double* inv_freq) {
+  for (int i = 0; i < r / 2; ++i) inv_freq[i] = pow(base, -2.0 * (double)i / (double)r);
+}
+
+/* Rotate-half rotary embedding of one head vector x[0..D) at position p:
+ *   for i < r/2 with theta = p * inv_freq[i]:
+ *     y[i]       = x[i] cos(theta) - x[i+r/2] sin(theta)
+ *     y[i+r/2]   = x[i+r/2] cos(theta) + x[i] sin(theta)
+ *   y[d] = x[d] for d >= r.                                                    */
+void neox_oracle_rotate(const double* x, int D, int r, double base, int64_t p, double* y) {
+  int h = r / 2;
+  for (int d = 0; d < D; ++d) y[d] = x[d];
+  for (int i = 0; i < h; ++i) {
+    double theta = (double)p * pow(base, -2.0 * (double)i / (double)r);
+    double c = cos(theta), s = sin(theta);
+    y[i] = x[i] * c - x[i + h] * s;
+    y[i + h] = x[i + h] * c + x[i] * s;
+  }
+}
+
+/* Element offset of qkv[b, s, h, slot, 0] in the packed [B,S,H,3,D] tensor. */
+static int64_t qkv_off(int64_t b, int64_t s, int64_t h, int slot, int S, int H, int D) {
+  return (((b * S + s) * H + h) * 3 + slot) * (int64_t)D;
+}
+
+typedef struct {
+  const uint16_t* qkv;
+  int B, S, H, D, r;
+  double base;
+  /* either all rows (rows == NULL) or the listed (b, h, i) triples */
+  const int64_t* rows;
+  int64_t n_rows;
+  const int64_t* order; /* rows sorted by (b, h): indices into rows */
+  double* out;
+  double* lse;
+  /* work distribution */
+  pthread_mutex_t mu;
+  int64_t next;
+  int64_t n_items;
+  int failed;
+} job_t;
+
+/* Rotated keys k'_s for s < n of head (b, h), plus raw values v_s. */
+static void load_head(const job_t* J, int64_t b, int64_t h, int64_t n, double* Kr, double* V, double* tmp) {
+  int D = J->D;
+  for (int64_t s = 0; s < n; ++s) {
+    const uint16_t* k = J->qkv + qkv_off(b, s, h, 1, J->S, J->H, D);
+    const uint16_t* v = J->qkv + qkv_off(b, s, h, 2, J->S, J->H, D);
+    for (int d = 0; d < D; ++d) tmp[d] = bf16_to_f64(k[d]);
+    neox_oracle_rotate(tmp, D, J->r, J->base, s, Kr + s * D);
+    for (int d = 0; d < D; ++d) V[s * D + d] = bf16_to_f64(v[d]);
+  }
+}
+
+/* One query row i of head (b, h): softmax over keys j <= i of q'_i.k'_j/sqrt(D).
+ * Writes out_row[0..D) and *lse_out.  scores has room for i+1 doubles.        */
+static void one_row(const job_t* J, int64_t b, int64_t h, int64_t i, const double* Kr, const double* V,
+                    double* qraw, double* qr, double* scores, double* out_row, double* lse_out) {
+  int D = J->D;
+  const uint16_t* q = J->qkv + qkv_off(b, i, h, 0, J->S, J->H, D);
+  for (int d = 0; d < D; ++d) qraw[d] = bf16_to_f64(q[d]);
+  neox_oracle_rotate(qraw, D, J->r, J->base, i, qr);
+  double scale = 1.0 / sqrt((double)D);
+  double m = -INFINITY;
+  for (int64_t j = 0; j <= i; ++j) {
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += qr[d] * Kr[j * D + d];
+    scores[j] = dot * scale;
+    if (scores[j] > m) m = scores[j];
+  }
+  double l = 0.0;
+  for (int64_t j = 0; j <= i; ++j) {
+    scores[j] = exp(scores[j] - m);
+    l += scores[j];
+  }
+  for (int d = 0; d < D; ++d) out_row[d] = 0.0;
+  for (int64_t j = 0; j <= i; ++j) {
+    double w = scores[j] / l;
+    for (int d = 0; d < D; ++d) out_row[d] += w * V[j * D + d];
+  }
+  *lse_out = m + log(l);
+}
+
+static int64_t take(job_t* J) {
+  pthread_mutex_lock(&J->mu);
+  int64_t k = J->next < J->n_items ? J->next++ : -1;
+  pthread_mutex_unlock(&J->mu);
+  return k;
+}
+
+/* Full mode: one work item = one head (b, h); every row of it. */
+static void* worker_full(void* arg) {
+  job_t* J = (job_t*)arg;
+  int S = J->S, H = J->H, D = J->D;
+  double* Kr = malloc(sizeof(double) * (size_t)S * D);
+  double* V = malloc(sizeof(double) * (size_t)S * D);
+  double* tmp = malloc(sizeof(double) * (size_t)D * 2);
+  double* scores = malloc(sizeof(double) * (size_t)S);
+  double* orow = malloc(sizeof(double) * (size_t)D);
+  if (!Kr || !V || !tmp || !scores || !orow) {
+    pthread_mutex_lock(&J->mu);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->mu);
+  } else {
+    for (int64_t item; (item = take(J)) >= 0;) {
+      int64_t b = item / H, h = item % H;
+      load_head(J, b, h, S, Kr, V, tmp);
+      for (int64_t i = 0; i < S; ++i) {
+        double l;
+        one_row(J, b, h, i, Kr, V, tmp, tmp + D, scores, orow, &l);
+        for (int d = 0; d < D; ++d) J->out[((b * S + i) * H + h) * D + d] = orow[d];
+        J->lse[(b * H + h) * S + i] = l;
+      }
+    }
+  }
+  free(Kr); free(V); free(tmp); free(scores); free(orow);
+  return NULL;
+}
+
+/* Rows mode: one work item = one head group of the (b,h)-sorted row list. */
+static void* worker_rows(void* arg) {
+  job_t* J = (job_t*)arg;
+  int S = J->S, D = J->D;
+  double* Kr = malloc(sizeof(double) * (size_t)S * D);
+  double* V = malloc(sizeof(double) * (size_t)S * D);
+  double* tmp = malloc(sizeof(double) * (size_t)D * 2);
+  double* scores = malloc(sizeof(double) * (size_t)S);
+  if (!Kr || !V || !tmp || !scores) {
+    pthread_mutex_lock(&J->mu);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->mu);
+  } else {
+    for (int64_t item; (item = take(J)) >= 0;) {
+      /* item indexes the sorted order; a group starts where (b,h) changes */
+      int64_t k0 = J->order[item];
+      int64_t b = J->rows[3 * k0], h = J->rows[3 * k0 + 1];
+      if (item > 0) {
+        int64_t kp = J->order[item - 1];
+        if (J->rows[3 * kp] == b && J->rows[3 * kp + 1] == h) continue; /* not a group start */
+      }
+      int64_t end = item, maxi = 0;
+      while (end < J->n_rows) {
+        int64_t k = J->order[end];
+        if (J->rows[3 * k] != b || J->rows[3 * k + 1] != h) break;
+        if (J->rows[3 * k + 2] > maxi) maxi = J->rows[3 * k + 2];
+        ++end;
+      }
+      load_head(J, b, h, maxi + 1, Kr, V, tmp);
+      for (int64_t e = item; e < end; ++e) {
+        int64_t k = J->order[e];
+        one_row(J, b, h, J->rows[3 * k + 2], Kr, V, tmp, tmp + D, scores, J->out + k * D, J->lse + k);
+      }
+    }
+  }
+  free(Kr); free(V); free(tmp); free(scores);
+  return NULL;
+}
+
+static int check_args(const uint16_t* qkv, int B, int S, int H, int D, int r, double base) {
+  if (!qkv || B < 1 || S < 1 || H < 1 || D < 1 || r < 0 || r > D || (r & 1) || !(base > 0.0)) return ORACLE_ERR_ARG;
+  return ORACLE_OK;
+}
+
+static int run(job_t* J, void* (*fn)(void*), int threads) {
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pthread_t tid[256];
+  pthread_mutex_init(&J->mu, NULL);
+  J->next = 0;
+  J->failed = 0;
+  int started = 0;
+  for (int t = 1; t < threads; ++t)
+    if (pthread_create(&tid[started], NULL, fn, J) == 0) ++started;
+  fn(J);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&J->mu);
+  return J->failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* Every row of every head.
+ * qkv: bf16 bits [B,S,H,3,D] (slot 0 = Q, 1 = K, 2 = V).
+ * out: fp64 [B,S,H,D];  lse: fp64 [B,H,S], natural log of the sum of exp of the
+ * scaled scores.  threads: worker threads (>= 1).  Returns 0 or a negative error. */
+int neox_oracle_fwd(const uint16_t* qkv, int B, int S, int H, int D, int r, double base,
+                    double* out, double* lse, int threads) {
+  int e = check_args(qkv, B, S, H, D, r, base);
+  if (e || !out || !lse) return ORACLE_ERR_ARG;
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.qkv = qkv; J.B = B; J.S = S; J.H = H; J.D = D; J.r = r; J.base = base;
+  J.out = out; J.lse = lse;
+  J.n_items = (int64_t)B * H;
+  return run(&J, worker_full, threads);
+}
+
+static const int64_t* g_sort_rows; /* only read inside the qsort call below */
+static int cmp_bh(const void* a, const void* b) {
+  int64_t i = *(const int64_t*)a, j = *(const int64_t*)b;
+  const int64_t* R = g_sort_rows;
+  if (R[3 * i] != R[3 * j]) return R[3 * i] < R[3 * j] ? -1 : 1;
+  if (R[3 * i + 1] != R[3 * j + 1]) return R[3 * i + 1] < R[3 * j + 1] ? -1 : 1;
+  return i < j ? -1 : (i > j);
+}
+static pthread_mutex_t g_sort_mu = PTHREAD_MUTEX_INITIALIZER;
+
+/* Listed rows only.  rows: n triples (b, h, i).  out: fp64 [n, D];  lse: fp64 [n]. */
+int neox_oracle_fwd_rows(const uint16_t* qkv, int B, int S, int H, int D, int r, double base,
+                         const int64_t* rows, int64_t n, double* out, double* lse, int threads) {
+  int e = check_args(qkv, B, S, H, D, r, base);
+  if (e || !rows || n < 0 || (n > 0 && (!out || !lse))) return ORACLE_ERR_ARG;
+  for (int64_t k = 0; k < n; ++k)
+    if (rows[3 * k] < 0 || rows[3 * k] >= B || rows[3 * k + 1] < 0 || rows[3 * k + 1] >= H ||
+        rows[3 * k + 2] < 0 || rows[3 * k + 2] >= S)
+      return ORACLE_ERR_ARG;
+  if (n == 0) return ORACLE_OK;
+  int64_t* order = malloc(sizeof(int64_t) * (size_t)n);
+  if (!order) return ORACLE_ERR_NOMEM;
+  for (int64_t k = 0; k < n; ++k) order[k] = k;
+  pthread_mutex_lock(&g_sort_mu);
+  g_sort_rows = rows;
+  qsort(order, (size_t)n, sizeof(int64_t), cmp_bh);
+  pthread_mutex_unlock(&g_sort_mu);
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.qkv = qkv; J.B = B; J.S = S; J.H = H; J.D = D; J.r = r; J.base = base;
+  J.rows = rows; J.n_rows = n; J.order = order; J.out = out; J.lse = lse;
+  J.n_items = n;
+  int rc = run(&J, worker_rows, threads);
+  free(order);
+  return rc;
+}
+
+/* The explicit probability row of query (b, h, i): p[j] = exp(s_ij - m) / l for
+ * j <= i.  p has room for i+1 doubles.  Used by the row-sum and weighting checks. */
+int neox_oracle_probs(const uint16_t* qkv, int B, int S, int H, int D, int r, double base,
+                      int b, int h, int i, double* p) {
+  int e = check_args(qkv, B, S, H, D, r, base);
+  if (e || !p || b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= S) return ORACLE_ERR_ARG;
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.qkv = qkv; J.B = B; J.S = S; J.H = H; J.D = D; J.r = r; J.base = base;
+  double* Kr = malloc(sizeof(double) * (size_t)(i + 1) * D);
+  double* V = malloc(sizeof(double) * (size_t)(i + 1) * D);
+  double* tmp = malloc(sizeof(double) * (size_t)D * 2);
+  double* orow = malloc(sizeof(double) * (size_t)D);
+  int rc = ORACLE_ERR_NOMEM;
+  if (Kr && V && tmp && orow) {
+    double l;
+    load_head(&J, b, h, i + 1, Kr, V, tmp);
+    one_row(&J, b, h, i, Kr, V, tmp, tmp + D, p, orow, &l);
+    /* one_row leaves exp(s_ij - m) in p; normalise by their sum */
+    double sum = 0.0;
+    for (int j = 0; j <= i; ++j) sum += p[j];
+    for (int j = 0; j <= i; ++j) p[j] /= sum;
+    rc = ORACLE_OK;
+  }
+  free(Kr); free(V); free(tmp); free(orow);
+  return rc;
+}

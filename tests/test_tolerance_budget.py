@@ -1,0 +1,108 @@
+"""Does the planned GPU arithmetic fit the parity tolerances?  (numpy, no GPU)
+
+The tolerances for unit-normal inputs are: bf16 output max abs error <= 2e-2,
+RMS <= 3e-3, lse max abs error <= 1e-3 (against the fp64 oracle).
+
+The kernel multiplies bf16 operands on the tensor cores with fp32 accumulation.
+The rotated Q/K dims come out of an fp32 rotation; rounding them to bf16 costs
+about 2^-9 relative per element, which on rows with few keys (row 0's lse is a
+single score) is too much.  The kernel therefore splits each rotated value into
+hi = bf16(y) and lo = bf16(y - hi) and accumulates q_hi.k_hi + q_hi.k_lo +
+q_lo.k_hi (the lo.lo term is ~2^-18 relative and dropped).  This test emulates
+both schemes around the oracle and shows that only the split one fits.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from causal_rope_self_neox_b300.workloads import bf16_bits, make_qkv
+
+OUT_MAX, OUT_RMS, LSE_MAX = 2e-2, 3e-3, 1e-3
+
+
+def bf16_round(x):
+    """fp32 -> bf16 round-to-nearest-even, returned as fp64."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def rotate_f32(x, r, base):
+    """fp32 rotation with an fp64-built, fp32-stored cos/sin table (the kernel's numerics)."""
+    S, D = x.shape
+    h = r // 2
+    y = x.astype(np.float32).copy()
+    if h == 0:
+        return y.astype(np.float64)
+    inv = base ** (-2.0 * np.arange(h) / r)
+    th = np.arange(S)[:, None] * inv[None, :]
+    c, s = np.cos(th).astype(np.float32), np.sin(th).astype(np.float32)
+    x1, x2 = x[:, :h].astype(np.float32), x[:, h:r].astype(np.float32)
+    y[:, :h] = x1 * c - x2 * s
+    y[:, h:r] = x2 * c + x1 * s
+    return y.astype(np.float64)
+
+
+def emulate(q, k, v, r, base, rows, split):
+    S, D = q.shape
+    qr, kr = rotate_f32(q, r, base), rotate_f32(k, r, base)
+    qh, kh = bf16_round(qr), bf16_round(kr)
+    if split:
+        ql, kl = bf16_round(qr - qh), bf16_round(kr - kh)
+    c = math.log2(math.e) / math.sqrt(D)
+    outs, lses = [], []
+    for i in rows:
+        s = kh[: i + 1] @ qh[i]
+        if split:
+            s = s + kl[: i + 1] @ qh[i] + kh[: i + 1] @ ql[i]
+        t = (s.astype(np.float32) * np.float32(c)).astype(np.float64)
+        m = t.max()
+        p = np.exp2(t - m).astype(np.float32).astype(np.float64)
+        l = float(np.float32(p.sum()))
+        o = (bf16_round(p) @ v[: i + 1]).astype(np.float32).astype(np.float64)
+        outs.append(bf16_round(o / l))
+        lses.append((m + math.log2(l)) * math.log(2.0))
+    return np.array(outs), np.array(lses)
+
+
+def errors(B, S, H, D, r, seed, k_scale, rows_per_head, split):
+    qkv = make_qkv(B, S, H, D, seed=seed, k_scale=k_scale)
+    x = qkv.double().numpy()
+    rng = np.random.default_rng(seed)
+    sel = []
+    for b in range(B):
+        for h in range(H):
+            rows = np.arange(S) if rows_per_head >= S else np.concatenate(
+                [[0, 1], np.sort(rng.choice(np.arange(2, S), rows_per_head - 2, replace=False))])
+            sel += [(b, h, int(i)) for i in rows]
+    ref_o, ref_l = oracle.fwd_rows(bf16_bits(qkv), B, S, H, D, r, 1e4, sel)
+    eo, el = [], []
+    for b in range(B):
+        for h in range(H):
+            idx = [k for k, t in enumerate(sel) if t[0] == b and t[1] == h]
+            rows = [sel[k][2] for k in idx]
+            o, l = emulate(x[b, :, h, 0], x[b, :, h, 1], x[b, :, h, 2], r, 1e4, rows, split)
+            eo.append(o - ref_o[idx])
+            el.append(l - ref_l[idx])
+    eo, el = np.concatenate(eo), np.concatenate(el)
+    return np.abs(eo).max(), math.sqrt((eo ** 2).mean()), np.abs(el).max()
+
+
+CASES = {  # name: (B, S, H, D, r, seed, k_scale, rows_per_head)
+    "tiny": (1, 128, 2, 64, 16, 1001, 1.0, 128),
+    "d96_r24": (1, 512, 1, 96, 24, 7, 1.0, 48),
+    "long_like": (1, 1024, 1, 128, 128, 9, 3.0, 32),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_split_scheme_fits_tolerances(name):
+    omax, orms, lmax = errors(*CASES[name], split=True)
+    assert omax <= OUT_MAX / 2 and orms <= OUT_RMS / 2 and lmax <= LSE_MAX / 10, (omax, orms, lmax)
+
+
+def test_plain_bf16_rotation_breaks_lse_tolerance():
+    _, _, lmax = errors(*CASES["tiny"], split=False)
+    assert lmax > LSE_MAX, lmax
