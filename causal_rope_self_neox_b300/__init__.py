@@ -1,0 +1,153 @@
+"""causal_rope_self_neox_b300 -- B300 (sm_103a) causal NeoX-rotary self-attention forward.
+
+The compute lives in the CUDA library ``libneox_attn.so`` (built in-tree from
+``csrc/`` by ``build.py``); this module is argument marshalling over its C ABI
+(``include/neox_attn.h``) with the same entry-point names, plus a torch
+convenience wrapper that allocates the outputs.  There is no CPU fallback: if the
+library is missing or the device is not a B300, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libneox_attn.so")
+
+NEOX_OK = 0
+NEOX_ERR_INVALID_ARG = -1
+NEOX_ERR_UNSUPPORTED_HEAD_DIM = -2
+NEOX_ERR_MISALIGNED = -3
+NEOX_ERR_CUDA = -4
+NEOX_ERR_DEVICE_TIMEOUT = -5
+NEOX_ERR_NO_DEVICE_SUPPORT = -6
+
+EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
+           "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
+           "neox_attn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class NeoxAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises OSError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise OSError(f"{path} is missing: build it with `python -m causal_rope_self_neox_b300.build`")
+            lib = ctypes.CDLL(path)
+            P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+            fwd_args = [P, i32, i32, i32, i32, i32, f32, P, P, P]
+            for name in ("neox_attn_fwd", "neox_attn_fwd_simple"):
+                getattr(lib, name).argtypes = fwd_args
+                getattr(lib, name).restype = i32
+            lib.neox_attn_get_device_error.argtypes = []
+            lib.neox_attn_get_device_error.restype = i32
+            lib.neox_attn_status_string.argtypes = [i32]
+            lib.neox_attn_status_string.restype = ctypes.c_char_p
+            lib.neox_attn_last_cuda_error.argtypes = []
+            lib.neox_attn_last_cuda_error.restype = i32
+            lib.neox_attn_release.argtypes = []
+            lib.neox_attn_release.restype = None
+            lib.neox_attn_selftest_wait_timeout.argtypes = [i64, P]
+            lib.neox_attn_selftest_wait_timeout.restype = i32
+            lib.neox_attn_version.argtypes = []
+            lib.neox_attn_version.restype = i32
+            _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------- raw C ABI ----
+
+def neox_attn_fwd(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
+                  out_ptr: int, lse_ptr: int, stream: int = 0) -> int:
+    """Raw call: device pointers and a cudaStream_t handle as integers; returns a status."""
+    return load_library().neox_attn_fwd(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr, stream)
+
+
+def neox_attn_fwd_simple(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
+                         out_ptr: int, lse_ptr: int, stream: int = 0) -> int:
+    return load_library().neox_attn_fwd_simple(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr,
+                                               stream)
+
+
+def neox_attn_get_device_error() -> int:
+    return load_library().neox_attn_get_device_error()
+
+
+def neox_attn_status_string(status: int) -> str:
+    return load_library().neox_attn_status_string(status).decode()
+
+
+def status_string(status: int) -> str:
+    try:
+        return neox_attn_status_string(status)
+    except OSError:
+        return "library not loaded"
+
+
+def neox_attn_last_cuda_error() -> int:
+    return load_library().neox_attn_last_cuda_error()
+
+
+def neox_attn_release() -> None:
+    load_library().neox_attn_release()
+
+
+def neox_attn_selftest_wait_timeout(timeout_ns: int, stream: int = 0) -> int:
+    return load_library().neox_attn_selftest_wait_timeout(timeout_ns, stream)
+
+
+def neox_attn_version() -> int:
+    return load_library().neox_attn_version()
+
+
+# ----------------------------------------------------- torch convenience ----
+
+def attn_fwd(qkv, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=None, stream=None,
+             kernel: str = "default"):
+    """Causal NeoX-rotary attention forward on CUDA tensors.
+
+    ``qkv``: bf16 ``[B, S, H, 3, D]`` contiguous on a CUDA device.  Returns
+    ``(out[B,S,H,D] bf16, lse[B,H,S] fp32)``; ``out``/``lse`` may be passed in.
+    torch only allocates memory and supplies the stream; the library computes.
+    """
+    import torch
+
+    if qkv.dim() != 5 or qkv.shape[3] != 3 or qkv.dtype != torch.bfloat16 or not qkv.is_cuda:
+        raise ValueError("qkv must be a CUDA bf16 tensor of shape [B, S, H, 3, D]")
+    if not qkv.is_contiguous():
+        raise ValueError("qkv must be contiguous")
+    B, S, H, _, D = qkv.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=qkv.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=qkv.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device)
+    fn = neox_attn_fwd if kernel == "default" else neox_attn_fwd_simple
+    with torch.cuda.device(qkv.device):
+        rc = fn(qkv.data_ptr(), B, S, H, D, rotary_dim, float(rotary_base), out.data_ptr(), lse.data_ptr(),
+                stream.cuda_stream)
+    if rc != NEOX_OK:
+        raise NeoxAttnError(rc, "neox_attn_fwd")
+    return out, lse
+
+
+def check_device_error() -> None:
+    """Raise if a kernel's bounded wait ran out since the last check (synchronizes first)."""
+    import torch
+
+    torch.cuda.synchronize()
+    rc = neox_attn_get_device_error()
+    if rc != NEOX_OK:
+        raise NeoxAttnError(rc, "device")

@@ -1,0 +1,68 @@
+// attn_common.cuh -- pieces shared by the attention kernels: parameters, the device error
+// word, bounded barrier waits and the row-softmax helpers.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "rotary.cuh"
+#include "tile_layout.cuh"
+
+namespace neox {
+
+// Error word (per device).  Bit 0: a bounded wait ran out.  Bits 8..15: the wait site.
+__device__ unsigned int g_device_error = 0;
+constexpr unsigned int kErrTimeout = 1u;
+
+// A wait that has not completed after this long is treated as a hang: the kernel records
+// it, stops its own work and exits cleanly instead of blocking the GPU.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct AttnParams {
+  const float2* cs;    // cos/sin table [>= S][r/2]
+  uint16_t* out;       // bf16 [B, S, H, D]
+  float* lse;          // fp32 [B, H, S]
+  int B, S, H, r;      // r = rotary_dim
+  int r16;             // r rounded up to a multiple of 16 (columns of lo products)
+  int side_cols;       // r16 rounded up to a multiple of 32 (side tile width), 0 if r == 0
+  float scale_log2;    // log2(e) / sqrt(D)
+  int num_units;       // work units (persistent kernel)
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void record_error(unsigned int code, unsigned int site) {
+  atomicOr(&g_device_error, code | (site << 8));
+}
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the limit ran
+// out (then the abort flag is raised and the error recorded).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns,
+                                           unsigned int site) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      record_error(kErrTimeout, site);
+      return false;
+    }
+  }
+}
+
+// Drain wait used on the abort path: waits for an in-flight async operation to land,
+// ignoring the abort flag, still bounded.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) break;
+  }
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) { return fmaxf(fmaxf(a, b), c); }
+
+}  // namespace neox

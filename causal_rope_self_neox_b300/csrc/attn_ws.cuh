@@ -1,0 +1,443 @@
+// attn_ws.cuh -- the persistent, warp-specialised causal rotary attention kernel.
+//
+// One CTA per SM (persistent).  A work unit is (b, h, t): the two 128-row query tiles
+// 2t and 2t+1 of one head, which share one stream of 128-key K/V blocks.  Units are
+// taken longest first (descending t) in a static stride over the CTAs.
+//
+// Roles (384 threads):
+//   warp 0        TMA producer: Q tiles once per unit, then K_j / V_j into rings
+//   warp 1        tcgen05 issuer (one lane) and TMEM owner
+//   warps 2-3     rotary transform: rotate-half of Q (per unit) and of K_j (per block)
+//                 in shared memory, hi in place, lo to the side tiles
+//   warps 4-7     softmax + lazy correction + epilogue of query tile 0
+//   warps 8-11    the same for query tile 1
+//
+// TMEM (512 columns): S/P of tile 0 at [0,128), S/P of tile 1 at [128,256),
+// O of tile 0 at [256, 256+D), O of tile 1 at [384, 384+D).  P (bf16) overwrites the
+// first 64 columns of its S block; the PV MMA reads it from TMEM as operand A.
+//
+// MMA order per block step j (for each tile tau with work):
+//   PV_tau(j-1): O_tau (+)= P_tau V_{j-1}, after softmax tau published P_tau(j-1)
+//   S_tau(j)   : S_tau  = Q'_tau K'_j^T   (commit -> s_full[tau])
+// so the softmax of one tile overlaps the MMAs of the other.  Because a commit tracks
+// every earlier MMA of the issuing thread, s_full[tau] for block j also means that
+// PV_tau(j-1) has landed: the softmax may rescale O_tau in place right then.
+//
+// Causality: tile q visits KV blocks 0..q only, and masks keys > row on block q.
+#pragma once
+
+#include "attn_common.cuh"
+
+namespace neox {
+
+constexpr int kWsThreads = 384;
+
+struct WsLayout {
+  int q_raw[2], q_side[2];
+  int k_raw[4], k_side[4];
+  int v[4];
+  int bars;
+  int total;
+};
+
+// Shared-memory carve-up; identical on host and device.
+__host__ __device__ inline WsLayout ws_layout(int D, int side_cols, int NK, int NV) {
+  WsLayout L{};
+  int off = 0;
+  for (int t = 0; t < 2; ++t) {
+    L.q_raw[t] = off; off += tile_bytes(D);
+    L.q_side[t] = off; off += tile_bytes(side_cols);
+  }
+  for (int s = 0; s < NK; ++s) {
+    L.k_raw[s] = off; off += tile_bytes(D);
+    L.k_side[s] = off; off += tile_bytes(side_cols);
+  }
+  for (int s = 0; s < NV; ++s) { L.v[s] = off; off += tile_bytes(D); }
+  L.bars = off;
+  off += 64 * 8 + 16;  // barriers, TMEM slot, abort flag
+  L.total = off + 1024;  // + alignment slack
+  return L;
+}
+
+// Barrier indices inside the barrier block.
+enum : int {
+  BAR_Q_FULL = 0, BAR_Q_READY = 1, BAR_Q_EMPTY = 2, BAR_DRAIN = 3,
+  BAR_S_FULL = 4,   // +tau
+  BAR_P_FULL = 6,   // +tau
+  BAR_O_FINAL = 8,  // +tau
+  BAR_K_FULL = 10,  // +slot (4)
+  BAR_K_READY = 14, // +slot
+  BAR_K_EMPTY = 18, // +slot
+  BAR_V_FULL = 22,  // +slot (4)
+  BAR_V_EMPTY = 26, // +slot
+  BAR_COUNT = 30
+};
+
+struct Unit {
+  int b, h, t;
+  int n0, n1;    // KV blocks of tile 0 / tile 1 (n1 = 0: no tile 1)
+  int nkv;       // max(n0, n1)
+};
+
+__device__ __forceinline__ Unit decode_unit(int k, int B, int H, int S) {
+  const int T = (S + 255) / 256;
+  const int bh_count = B * H;
+  Unit u;
+  u.t = T - 1 - k / bh_count;
+  const int bh = k % bh_count;
+  u.b = bh / H;
+  u.h = bh % H;
+  u.n0 = 2 * u.t + 1;
+  u.n1 = ((2 * u.t + 1) * kRows < S) ? 2 * u.t + 2 : 0;
+  u.nkv = u.n1 > u.n0 ? u.n1 : u.n0;
+  return u;
+}
+
+template <int D, int NK, int NV>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const WsLayout L = ws_layout(D, p.side_cols, NK, NV);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint64_t lim = p.wait_limit_ns;
+
+  // ---------------------------------------------------------------- setup ----
+  if (tid == 0) {
+    mbar_init(bar(BAR_Q_FULL), 1);
+    mbar_init(bar(BAR_Q_READY), 64);
+    mbar_init(bar(BAR_Q_EMPTY), 1);
+    mbar_init(bar(BAR_DRAIN), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(BAR_S_FULL + t), 1);
+      mbar_init(bar(BAR_P_FULL + t), 128);
+      mbar_init(bar(BAR_O_FINAL + t), 1);
+    }
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(bar(BAR_K_FULL + s), 1);
+      mbar_init(bar(BAR_K_READY + s), 64);
+      mbar_init(bar(BAR_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(bar(BAR_V_FULL + s), 1);
+      mbar_init(bar(BAR_V_EMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  // side tiles start at zero; columns >= r are never written again
+  if (p.side_cols > 0) {
+    const int sb = tile_bytes(p.side_cols);
+    for (int i = tid * 16; i < sb; i += kWsThreads * 16) {
+      for (int t = 0; t < 2; ++t) *reinterpret_cast<uint4*>(smem + L.q_side[t] + i) = make_uint4(0, 0, 0, 0);
+      for (int s = 0; s < NK; ++s) *reinterpret_cast<uint4*>(smem + L.k_side[s] + i) = make_uint4(0, 0, 0, 0);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const int G = gridDim.x;
+  if (warp == 0) {
+    // ============================================================ producer ====
+    if (lane == 0) {
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      uint32_t kfill = 0, vfill = 0, u_local = 0;
+      int last_k_par[NK], last_v_par[NV];
+      for (int s = 0; s < NK; ++s) last_k_par[s] = -1;
+      for (int s = 0; s < NV; ++s) last_v_par[s] = -1;
+      int last_q_par = -1;
+      bool ok = true;
+      for (int k = blockIdx.x; k < p.num_units && ok; k += G, ++u_local) {
+        const Unit u = decode_unit(k, p.B, p.H, p.S);
+        if (!wait_phase(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_flag, lim, 10)) { ok = false; break; }
+        const int qbytes = tile_bytes(D) * (u.n1 > 0 ? 2 : 1);
+        mbar_arrive_expect_tx(bar(BAR_Q_FULL), qbytes);
+        last_q_par = u_local & 1;
+        for (int t = 0; t < (u.n1 > 0 ? 2 : 1); ++t)
+          for (int cb = 0; cb < D / kBlkCols; ++cb)
+            tma_load_4d_hint(smem_u32(smem + L.q_raw[t] + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
+                             3 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
+        // K_j before V_{j-1}: the order in which the MMA warp consumes them
+        for (int j = 0; j <= u.nkv && ok; ++j) {
+          if (j < u.nkv) {
+            const int s = kfill % NK;
+            if (!wait_phase(bar(BAR_K_EMPTY + s), ((kfill / NK) & 1) ^ 1, abort_flag, lim, 11)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D));
+            last_k_par[s] = (kfill / NK) & 1;
+            for (int cb = 0; cb < D / kBlkCols; ++cb)
+              tma_load_4d_hint(smem_u32(smem + L.k_raw[s] + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s),
+                               cb * kBlkCols, 3 * u.h + 1, j * kRows, u.b, pol_kv);
+            ++kfill;
+          }
+          if (j >= 1) {
+            const int s = vfill % NV;
+            if (!wait_phase(bar(BAR_V_EMPTY + s), ((vfill / NV) & 1) ^ 1, abort_flag, lim, 12)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar(BAR_V_FULL + s), tile_bytes(D));
+            last_v_par[s] = (vfill / NV) & 1;
+            for (int cb = 0; cb < D / kBlkCols; ++cb)
+              tma_load_4d_hint(smem_u32(smem + L.v[s] + cb * kBlkBytes), &tmap, bar(BAR_V_FULL + s), cb * kBlkCols,
+                               3 * u.h + 2, (j - 1) * kRows, u.b, pol_kv);
+            ++vfill;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        // let every load this thread armed land before the CTA's shared memory goes away
+        if (last_q_par >= 0) drain_phase(bar(BAR_Q_FULL), last_q_par, lim);
+        for (int s = 0; s < NK; ++s) if (last_k_par[s] >= 0) drain_phase(bar(BAR_K_FULL + s), last_k_par[s], lim);
+        for (int s = 0; s < NV; ++s) if (last_v_par[s] >= 0) drain_phase(bar(BAR_V_FULL + s), last_v_par[s], lim);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================================================ MMA issuer ====
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
+      uint32_t kuse = 0, vuse = 0, u_local = 0;
+      uint32_t p_cnt[2] = {0, 0};
+      bool ok = true, issued = false;
+      for (int k = blockIdx.x; k < p.num_units && ok; k += G, ++u_local) {
+        const Unit u = decode_unit(k, p.B, p.H, p.S);
+        if (!wait_phase(bar(BAR_Q_READY), u_local & 1, abort_flag, lim, 30)) { ok = false; break; }
+        tc_fence_after_sync();
+        for (int j = 0; j <= u.nkv && ok; ++j) {
+          int ks = 0, vs = 0;
+          if (j < u.nkv) {
+            ks = kuse % NK;
+            if (!wait_phase(bar(BAR_K_READY + ks), (kuse / NK) & 1, abort_flag, lim, 31)) { ok = false; break; }
+          }
+          if (j >= 1) {
+            vs = vuse % NV;
+            if (!wait_phase(bar(BAR_V_FULL + vs), (vuse / NV) & 1, abort_flag, lim, 32)) { ok = false; break; }
+          }
+          tc_fence_after_sync();
+          for (int tau = 0; tau < 2; ++tau) {
+            const int n = tau == 0 ? u.n0 : u.n1;
+            if (n == 0) continue;
+            const uint32_t tS = tmem + tau * 128, tO = tmem + 256 + tau * 128;
+            if (j >= 1 && j <= n) {
+              if (!wait_phase(bar(BAR_P_FULL + tau), p_cnt[tau] & 1, abort_flag, lim, 33)) { ok = false; break; }
+              ++p_cnt[tau];
+              tc_fence_after_sync();
+              const uint32_t vaddr = smem_u32(smem + L.v[vs]);
+#pragma unroll
+              for (int kk = 0; kk < kRows / 16; ++kk)
+                mma_ts(tO, tS + kk * 8, vmajor_desc(vaddr, kk), idesc_pv, (j > 1 || kk > 0));
+              issued = true;
+              if (j == n) tc_commit(bar(BAR_O_FINAL + tau));
+            }
+            if (j < n) {
+              const uint32_t q = smem_u32(smem + L.q_raw[tau]), qs = smem_u32(smem + L.q_side[tau]);
+              const uint32_t kr = smem_u32(smem + L.k_raw[ks]), ksd = smem_u32(smem + L.k_side[ks]);
+#pragma unroll
+              for (int kc = 0; kc < D / 16; ++kc) mma_ss(tS, kmajor_desc(q, kc), kmajor_desc(kr, kc), idesc_s, kc > 0);
+              for (int kc = 0; kc < p.r16 / 16; ++kc) {
+                mma_ss(tS, kmajor_desc(qs, kc), kmajor_desc(kr, kc), idesc_s, 1);
+                mma_ss(tS, kmajor_desc(q, kc), kmajor_desc(ksd, kc), idesc_s, 1);
+              }
+              issued = true;
+              tc_commit(bar(BAR_S_FULL + tau));
+            }
+          }
+          if (!ok) break;
+          if (j < u.nkv) { tc_commit(bar(BAR_K_EMPTY + ks)); ++kuse; }
+          if (j >= 1) { tc_commit(bar(BAR_V_EMPTY + vs)); ++vuse; }
+        }
+        tc_commit(bar(BAR_Q_EMPTY));
+      }
+      if (issued && (!ok || *abort_flag)) {
+        tc_commit(bar(BAR_DRAIN));
+        drain_phase(bar(BAR_DRAIN), 0, lim);
+      }
+    }
+  } else if (warp < 4) {
+    // ======================================================= rotary transform ====
+    const int tt = tid - 64;  // 0..63: rows tt and tt + 64
+    uint32_t kuse = 0, u_local = 0;
+    for (int k = blockIdx.x; k < p.num_units; k += G, ++u_local) {
+      const Unit u = decode_unit(k, p.B, p.H, p.S);
+      if (!wait_phase(bar(BAR_Q_FULL), u_local & 1, abort_flag, lim, 20)) break;
+      if (p.r > 0) {
+        for (int t = 0; t < (u.n1 > 0 ? 2 : 1); ++t)
+          for (int rr = 0; rr < 2; ++rr) {
+            const int row = tt + rr * 64;
+            const int64_t pos = static_cast<int64_t>(2 * u.t + t) * kRows + row;
+            rotate_row(smem + L.q_raw[t], smem + L.q_side[t], row, pos < p.S ? pos : -1, p.cs, p.r);
+          }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(BAR_Q_READY));
+      bool ok = true;
+      for (int j = 0; j < u.nkv; ++j) {
+        const int s = kuse % NK;
+        if (!wait_phase(bar(BAR_K_FULL + s), (kuse / NK) & 1, abort_flag, lim, 21)) { ok = false; break; }
+        if (p.r > 0) {
+          for (int rr = 0; rr < 2; ++rr) {
+            const int row = tt + rr * 64;
+            const int64_t pos = static_cast<int64_t>(j) * kRows + row;
+            rotate_row(smem + L.k_raw[s], smem + L.k_side[s], row, pos < p.S ? pos : -1, p.cs, p.r);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(BAR_K_READY + s));
+        ++kuse;
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ========================================== softmax / correction / epilogue ====
+    const int tau = (warp - 4) >> 2;          // query tile of this warpgroup
+    const int row = tid - 128 * (tau + 1);     // 0..127: this thread's row / TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + tau * 128 + lane_off, tO = tmem + 256 + tau * 128 + lane_off;
+    const float sl2 = p.scale_log2;
+    uint32_t s_use = 0, o_use = 0;
+    for (int k = blockIdx.x; k < p.num_units; k += G) {
+      const Unit u = decode_unit(k, p.B, p.H, p.S);
+      const int n = tau == 0 ? u.n0 : u.n1;
+      if (n == 0) continue;
+      const int qt = 2 * u.t + tau;
+      float m_used = -INFINITY, l_run = 0.0f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (!wait_phase(bar(BAR_S_FULL + tau), s_use & 1, abort_flag, lim, 40)) { ok = false; break; }
+        ++s_use;
+        tc_fence_after_sync();
+        uint32_t sr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
+        tmem_wait_ld();
+        if (j == qt) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > row) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        const float mx_s = mx * sl2;
+        float m_new = m_used;
+        bool rescale = false;
+        if (j == 0) {
+          m_new = mx_s;
+        } else if (mx_s > m_used + 8.0f) {
+          m_new = mx_s;
+          rescale = true;
+        }
+        const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.0f;
+        float rowsum = 0.0f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_new));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_new));
+          rowsum += p0 + p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l_run = l_run * alpha + rowsum;
+        m_used = m_new;
+        // lazy correction: O holds sum over blocks < j (landed, see s_full); rescale it only
+        // when some row's running max grew by more than 2^8
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+            tmem_st32(tO + c0, o);
+          }
+        }
+        tmem_st32(tS, pk);
+        tmem_st32(tS + 32, pk + 32);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bar(BAR_P_FULL + tau));
+      }
+      if (!ok) break;
+      if (!wait_phase(bar(BAR_O_FINAL + tau), o_use & 1, abort_flag, lim, 41)) break;
+      ++o_use;
+      tc_fence_after_sync();
+      const int qrow = qt * kRows + row;
+      const float inv_l = 1.0f / l_run;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          pk[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv_l, __uint_as_float(o[2 * q + 1]) * inv_l);
+        if (qrow < p.S) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(u.b) * p.S + qrow) * p.H + u.h) * D + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (qrow < p.S)
+        p.lse[(static_cast<int64_t>(u.b) * p.H + u.h) * p.S + qrow] = (m_used + log2f(l_run)) * 0.69314718055994530942f;
+      tc_fence_before_sync();
+    }
+  }
+
+  // ------------------------------------------------------------- teardown ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Ring depths per head dim (shared memory <= 227 KB with the side tiles of r <= 64).
+template <int D>
+struct WsConfig;
+template <> struct WsConfig<64> { static constexpr int NK = 4, NV = 4; };
+template <> struct WsConfig<96> { static constexpr int NK = 3, NV = 2; };
+template <> struct WsConfig<128> { static constexpr int NK = 2, NV = 2; };
+
+template <int D, int NK, int NV>
+int launch_ws_impl(const CUtensorMap& map, AttnParams p, int num_sms, cudaStream_t stream, int* last_err) {
+  const WsLayout L = ws_layout(D, p.side_cols, NK, NV);
+  auto kern = attn_fwd_ws_kernel<D, NK, NV>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
+  const int T = (p.S + 255) / 256;
+  p.num_units = p.B * p.H * T;
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  kern<<<grid, kWsThreads, L.total, stream>>>(map, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
+  return 0;
+}
+
+constexpr int kSmemLimit = 227 * 1024;
+
+// Picks ring depths that fit: the configured ones, else shallower rings for wide side tiles.
+template <int D>
+int launch_attn_ws(const CUtensorMap& map, const AttnParams& p, int num_sms, cudaStream_t stream, int* last_err) {
+  constexpr int NK = WsConfig<D>::NK, NV = WsConfig<D>::NV;
+  if (ws_layout(D, p.side_cols, NK, NV).total <= kSmemLimit) return launch_ws_impl<D, NK, NV>(map, p, num_sms, stream, last_err);
+  if (ws_layout(D, p.side_cols, 2, 2).total <= kSmemLimit) return launch_ws_impl<D, 2, 2>(map, p, num_sms, stream, last_err);
+  if (ws_layout(D, p.side_cols, 2, 1).total <= kSmemLimit) return launch_ws_impl<D, 2, 1>(map, p, num_sms, stream, last_err);
+  return launch_ws_impl<D, 1, 1>(map, p, num_sms, stream, last_err);
+}
+
+}  // namespace neox

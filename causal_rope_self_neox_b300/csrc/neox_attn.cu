@@ -1,0 +1,311 @@
+// neox_attn.cu -- the C ABI (include/neox_attn.h): argument validation, the cached
+// cos/sin table, TMA descriptor encoding and kernel launch.  No torch types anywhere.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "neox_attn.h"
+#include "attn_common.cuh"
+#include "attn_simple.cuh"
+#include "attn_ws.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return NEOX_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- validation ----
+bool ranges_overlap(uintptr_t a, uint64_t na, uintptr_t b, uint64_t nb) { return a < b + nb && b < a + na; }
+
+int validate(const void* qkv, int B, int S, int H, int D, int r, float base, const void* out, const float* lse) {
+  if (!qkv || !out || !lse) return NEOX_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1) return NEOX_ERR_INVALID_ARG;
+  if (D != 64 && D != 96 && D != 128) return NEOX_ERR_UNSUPPORTED_HEAD_DIM;
+  if (r < 0 || r > D || (r & 1)) return NEOX_ERR_INVALID_ARG;
+  if (!(base > 0.0f) || !std::isfinite(base)) return NEOX_ERR_INVALID_ARG;
+  const uint64_t elems = static_cast<uint64_t>(B) * S * H * 3 * D;
+  if (elems >= (1ull << 40)) return NEOX_ERR_INVALID_ARG;
+  if (static_cast<uint64_t>(B) * H > 0x7FFFFFFFull) return NEOX_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(out) & 15)) return NEOX_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3) return NEOX_ERR_MISALIGNED;
+  const uint64_t qkv_bytes = elems * 2, out_bytes = elems / 3 * 2, lse_bytes = static_cast<uint64_t>(B) * H * S * 4;
+  const uintptr_t q = reinterpret_cast<uintptr_t>(qkv), o = reinterpret_cast<uintptr_t>(out),
+                  l = reinterpret_cast<uintptr_t>(lse);
+  if (ranges_overlap(q, qkv_bytes, o, out_bytes) || ranges_overlap(q, qkv_bytes, l, lse_bytes) ||
+      ranges_overlap(o, out_bytes, l, lse_bytes))
+    return NEOX_ERR_INVALID_ARG;
+  return NEOX_OK;
+}
+
+// --------------------------------------------------------- device properties ----
+struct DeviceInfo {
+  bool known = false;
+  bool supported = false;
+  int num_sms = 0;
+  bool smem_configured = false;
+};
+std::mutex g_dev_mu;
+std::vector<DeviceInfo> g_devs;
+
+int current_device(int* dev, DeviceInfo* info) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (static_cast<int>(g_devs.size()) <= *dev) g_devs.resize(*dev + 1);
+  DeviceInfo& d = g_devs[*dev];
+  if (!d.known) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, *dev)) != cudaSuccess) return cuda_fail(e);
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    d.known = true;
+  }
+  *info = d;
+  return d.supported ? NEOX_OK : NEOX_ERR_NO_DEVICE_SUPPORT;
+}
+
+// ------------------------------------------------------------ cos/sin tables ----
+struct Table {
+  int device;
+  int r;
+  float base;
+  int64_t rows;  // positions covered
+  float2* ptr;
+};
+std::mutex g_tab_mu;
+std::vector<Table> g_tables;
+
+int get_table(int device, int S, int r, float base, cudaStream_t stream, const float2** out) {
+  std::lock_guard<std::mutex> lk(g_tab_mu);
+  for (auto it = g_tables.begin(); it != g_tables.end(); ++it) {
+    if (it->device == device && it->r == r && it->base == base) {
+      if (it->rows >= S) {
+        *out = it->ptr;
+        return NEOX_OK;
+      }
+      // too short: in-flight kernels may still read it, so let the device go idle first
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return cuda_fail(e);
+      cudaFree(it->ptr);
+      g_tables.erase(it);
+      break;
+    }
+  }
+  const int h = r / 2;
+  const int64_t rows = ((static_cast<int64_t>(S) + 2047) / 2048) * 2048;
+  float2* ptr = nullptr;
+  cudaError_t e = cudaMalloc(&ptr, sizeof(float2) * rows * h);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int64_t n = rows * h;
+  const int threads = 256;
+  const int blocks = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 65535));
+  neox::rope_table_kernel<<<blocks, threads, 0, stream>>>(ptr, static_cast<int>(rows), h, r, static_cast<double>(base));
+  if ((e = cudaGetLastError()) != cudaSuccess || (e = cudaStreamSynchronize(stream)) != cudaSuccess) {
+    cudaFree(ptr);
+    return cuda_fail(e);
+  }
+  g_tables.push_back(Table{device, r, base, rows, ptr});
+  *out = ptr;
+  return NEOX_OK;
+}
+
+// -------------------------------------------------------------- tensor maps ----
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return cuda_fail(cudaErrorNotSupported);
+  // dims (innermost first): head dim, (head, slot), sequence, batch.
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(3) * H, static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(3) * H * D * 2,
+                           static_cast<cuuint64_t>(S) * 3 * H * D * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(neox::kBlkCols), 1, static_cast<cuuint32_t>(neox::kRows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(qkv), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return NEOX_OK;
+}
+
+// ------------------------------------------------------------------ launches ----
+struct Prepared {
+  CUtensorMap map;
+  neox::AttnParams p;
+  DeviceInfo dev;
+  int device;
+};
+
+int prepare(const void* qkv, int B, int S, int H, int D, int r, float base, void* out, float* lse, cudaStream_t stream,
+            Prepared* P) {
+  int rc = validate(qkv, B, S, H, D, r, base, out, lse);
+  if (rc != NEOX_OK) return rc;
+  rc = current_device(&P->device, &P->dev);
+  if (rc != NEOX_OK) return rc;
+  const float2* cs = nullptr;
+  if (r > 0) {
+    rc = get_table(P->device, S, r, base, stream, &cs);
+    if (rc != NEOX_OK) return rc;
+  }
+  rc = encode_qkv_map(&P->map, qkv, B, S, H, D);
+  if (rc != NEOX_OK) return rc;
+  neox::AttnParams& p = P->p;
+  p.cs = cs;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.r = r;
+  p.r16 = (r + 15) / 16 * 16;
+  p.side_cols = r > 0 ? (p.r16 + 31) / 32 * 32 : 0;
+  p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  p.num_units = 0;
+  p.wait_limit_ns = neox::kWaitLimitNs;
+  return NEOX_OK;
+}
+
+template <int D>
+int launch_simple(const Prepared& P, cudaStream_t stream) {
+  const int smem = neox::simple_smem_bytes(D, P.p.side_cols);
+  cudaError_t e = cudaFuncSetAttribute(neox::attn_fwd_simple_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (P.p.H > 65535 || P.p.B > 65535) return NEOX_ERR_INVALID_ARG;
+  dim3 grid((P.p.S + neox::kRows - 1) / neox::kRows, P.p.H, P.p.B);
+  neox::attn_fwd_simple_kernel<D><<<grid, 128, smem, stream>>>(P.map, P.p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
+}
+
+template <int D>
+int launch_ws(Prepared& P, cudaStream_t stream) {
+  const int rc = neox::launch_attn_ws<D>(P.map, P.p, P.dev.num_sms, stream, &g_last_cuda_error);
+  return rc == 0 ? NEOX_OK : NEOX_ERR_CUDA;
+}
+
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    neox::mbar_init(neox::smem_u32(&bar), 1);
+    abort_flag = 0;
+    neox::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) neox::wait_phase(neox::smem_u32(&bar), 0, &abort_flag, limit_ns, 0xEE);
+}
+
+}  // namespace
+
+extern "C" {
+
+int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out, float* lse,
+                  void* stream) {
+  try {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Prepared P;
+    int rc = prepare(qkv, B, S, H, D, rotary_dim, rotary_base, out, lse, st, &P);
+    if (rc != NEOX_OK) return rc;
+    switch (D) {
+      case 64: return launch_ws<64>(P, st);
+      case 96: return launch_ws<96>(P, st);
+      default: return launch_ws<128>(P, st);
+    }
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
+
+int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out,
+                         float* lse, void* stream) {
+  try {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Prepared P;
+    int rc = prepare(qkv, B, S, H, D, rotary_dim, rotary_base, out, lse, st, &P);
+    if (rc != NEOX_OK) return rc;
+    switch (D) {
+      case 64: return launch_simple<64>(P, st);
+      case 96: return launch_simple<96>(P, st);
+      default: return launch_simple<128>(P, st);
+    }
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
+
+int neox_attn_get_device_error(void) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, neox::g_device_error, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v == 0) return NEOX_OK;
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(neox::g_device_error, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return NEOX_ERR_DEVICE_TIMEOUT;
+}
+
+const char* neox_attn_status_string(int status) {
+  switch (status) {
+    case NEOX_OK: return "ok";
+    case NEOX_ERR_INVALID_ARG: return "invalid argument";
+    case NEOX_ERR_UNSUPPORTED_HEAD_DIM: return "unsupported head dim (64, 96 or 128)";
+    case NEOX_ERR_MISALIGNED: return "misaligned pointer";
+    case NEOX_ERR_CUDA: return "CUDA error";
+    case NEOX_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case NEOX_ERR_NO_DEVICE_SUPPORT: return "device is not compute capability 10.3";
+    default: return "unknown status";
+  }
+}
+
+int neox_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+void neox_attn_release(void) {
+  std::lock_guard<std::mutex> lk(g_tab_mu);
+  if (!g_tables.empty()) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& t : g_tables) {
+      cudaSetDevice(t.device);
+      cudaDeviceSynchronize();
+      cudaFree(t.ptr);
+    }
+    cudaSetDevice(cur);
+    g_tables.clear();
+  }
+}
+
+int neox_attn_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000 || timeout_ns > 1000000000) return NEOX_ERR_INVALID_ARG;
+  int dev = 0;
+  DeviceInfo info;
+  int rc = current_device(&dev, &info);
+  if (rc != NEOX_OK) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(timeout_ns));
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
+}
+
+int neox_attn_version(void) { return 100; }
+
+}  // extern "C"

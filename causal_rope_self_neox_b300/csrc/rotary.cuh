@@ -1,0 +1,98 @@
+// rotary.cuh -- NeoX rotate-half rotary embedding on shared-memory tiles.
+//
+// The rotation (GPT-NeoX on FasterTransformer guide, sections "背景" and "模型配置":
+// Neox-style rotary on both Query and Key, rotary_embedding of the head dims) pairs dim i
+// with dim i + r/2 for i < r/2 and turns the pair by the angle p * base^(-2i/r), p the
+// token position.  Dims >= r pass through.
+//
+// The kernel keeps the tensor-core operands in bf16.  A rotated value y is computed in
+// fp32 and split as hi = bf16(y), lo = bf16(y - hi); the score is then accumulated as
+// q_hi.k_hi + q_hi.k_lo + q_lo.k_hi over the rotated dims (relative error ~2^-16, the
+// lo.lo term ~2^-18 is dropped), while a plain bf16 rounding of y (~2^-9) would cost up
+// to ~3e-3 in the row logsumexp.  "hi" overwrites y's slot in the tile itself; "lo" goes
+// to a side tile whose columns >= r stay zero.
+#pragma once
+
+#include <cstdint>
+
+#include "tile_layout.cuh"
+
+namespace neox {
+
+// cos/sin table, fp64 arithmetic stored as fp32: tab[p * h + i] = (cos, sin)(p * base^(-2i/r)).
+__global__ void rope_table_kernel(float2* __restrict__ tab, int S, int h, int r, double base) {
+  const int64_t n = static_cast<int64_t>(S) * h;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t p = idx / h;
+    const int i = static_cast<int>(idx - p * h);
+    const double inv_freq = pow(base, -2.0 * static_cast<double>(i) / static_cast<double>(r));
+    double s, c;
+    sincos(static_cast<double>(p) * inv_freq, &s, &c);
+    tab[idx] = make_float2(static_cast<float>(c), static_cast<float>(s));
+  }
+}
+
+__device__ __forceinline__ void split_hi_lo(float y, uint16_t& hi, uint16_t& lo) {
+  hi = f32_to_bf16_bits(y);
+  lo = f32_to_bf16_bits(y - bf16_bits_to_f32(hi));
+}
+
+// Rotate the first r dims of one tile row in place (hi) and write lo to the side tile.
+// pos < 0 marks a row past the end of the sequence (TMA filled it with zeros): lo = 0.
+__device__ __forceinline__ void rotate_row(uint8_t* tile, uint8_t* side, int row, int64_t pos,
+                                           const float2* __restrict__ cs, int r) {
+  const int h = r >> 1;
+  if ((h & 1) == 0) {
+    // two pairs per step with 32-bit shared accesses: (i, i+1) and (i+h, i+h+1)
+    for (int i = 0; i < h; i += 2) {
+      uint32_t* pa = reinterpret_cast<uint32_t*>(tile + sw64_off(row, i));
+      uint32_t* pb = reinterpret_cast<uint32_t*>(tile + sw64_off(row, i + h));
+      const uint32_t a = *pa, b = *pb;
+      float x0 = bf16_bits_to_f32(static_cast<uint16_t>(a & 0xFFFF));
+      float x1 = bf16_bits_to_f32(static_cast<uint16_t>(a >> 16));
+      float z0 = bf16_bits_to_f32(static_cast<uint16_t>(b & 0xFFFF));
+      float z1 = bf16_bits_to_f32(static_cast<uint16_t>(b >> 16));
+      float y0 = x0, y1 = x1, w0 = z0, w1 = z1;
+      if (pos >= 0) {
+        const float4 t = *reinterpret_cast<const float4*>(cs + pos * h + i);  // (c0, s0, c1, s1)
+        y0 = fmaf(x0, t.x, -z0 * t.y);
+        w0 = fmaf(z0, t.x, x0 * t.y);
+        y1 = fmaf(x1, t.z, -z1 * t.w);
+        w1 = fmaf(z1, t.z, x1 * t.w);
+      }
+      uint16_t hy0, ly0, hy1, ly1, hw0, lw0, hw1, lw1;
+      split_hi_lo(y0, hy0, ly0);
+      split_hi_lo(y1, hy1, ly1);
+      split_hi_lo(w0, hw0, lw0);
+      split_hi_lo(w1, hw1, lw1);
+      *pa = static_cast<uint32_t>(hy0) | (static_cast<uint32_t>(hy1) << 16);
+      *pb = static_cast<uint32_t>(hw0) | (static_cast<uint32_t>(hw1) << 16);
+      *reinterpret_cast<uint32_t*>(side + sw64_off(row, i)) =
+          static_cast<uint32_t>(ly0) | (static_cast<uint32_t>(ly1) << 16);
+      *reinterpret_cast<uint32_t*>(side + sw64_off(row, i + h)) =
+          static_cast<uint32_t>(lw0) | (static_cast<uint32_t>(lw1) << 16);
+    }
+  } else {
+    for (int i = 0; i < h; ++i) {
+      uint16_t* pa = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i));
+      uint16_t* pb = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i + h));
+      const float x = bf16_bits_to_f32(*pa), z = bf16_bits_to_f32(*pb);
+      float y = x, w = z;
+      if (pos >= 0) {
+        const float2 t = cs[pos * h + i];
+        y = fmaf(x, t.x, -z * t.y);
+        w = fmaf(z, t.x, x * t.y);
+      }
+      uint16_t hy, ly, hw, lw;
+      split_hi_lo(y, hy, ly);
+      split_hi_lo(w, hw, lw);
+      *pa = hy;
+      *pb = hw;
+      *reinterpret_cast<uint16_t*>(side + sw64_off(row, i)) = ly;
+      *reinterpret_cast<uint16_t*>(side + sw64_off(row, i + h)) = lw;
+    }
+  }
+}
+
+}  // namespace neox

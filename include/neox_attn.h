@@ -1,0 +1,121 @@
+/*
+ * neox_attn.h -- C ABI of the B300 (sm_103a) causal NeoX-rotary self-attention
+ * forward.
+ *
+ * The operation (defined from these pages):
+ *   - "GPT-NeoX on FasterTransformer" guide, section "背景": GPT-NeoX uses the
+ *     Neox-style rotary embedding (neox_rotary_style_ = true) and the context
+ *     attention accumulates Q.K^T in fp32 by default (is_context_qk_buf_float_).
+ *   - same guide, section "模型配置（config.ini）": rotary_embedding=24 of
+ *     size_per_head=96, with the rotation applied to both Query and Key.
+ *   - same guide, section "从 HuggingFace 检查点部署": the fused
+ *     query_key_value weight is laid out [hidden, num_heads, 3, head_hidden], so a
+ *     token's projection output is packed [H, 3, D]; this op reads that packed
+ *     tensor directly.
+ *   - "gpt-neox - 模型与框架" hub page, section "问题二：注意力计算太慢": the
+ *     attention is exact (Flash Attention 2 changes memory traffic, not results).
+ *
+ * For every batch b, head h and query position i (0-based; positions are the
+ * token indices 0..S-1, identical for Q and K):
+ *   q' = R(i) q_i,  k'_j = R(j) k_j, where R(p) rotates each pair (d, d + r/2),
+ *        d < r/2, by the angle p * rotary_base^(-2d/r) ("rotate-half"):
+ *        y_d = x_d cos - x_{d+r/2} sin,  y_{d+r/2} = x_{d+r/2} cos + x_d sin;
+ *        dims >= r pass through.  V is not rotated.
+ *   s_ij = q'.k'_j / sqrt(D) for j <= i (causal, diagonal kept),
+ *   out_i = sum_j softmax_j(s_ij) v_j,   lse_i = ln sum_j exp(s_ij).
+ *
+ * Threading: every entry point may be called from any host thread.  All work is
+ * stream-ordered on the caller's stream and asynchronous unless stated.
+ * No entry point throws across the ABI; errors come back as neox_status codes.
+ */
+#ifndef NEOX_ATTN_H_
+#define NEOX_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  NEOX_OK = 0,
+  NEOX_ERR_INVALID_ARG = -1,          /* null pointer, bad size, overlap of out/lse with qkv */
+  NEOX_ERR_UNSUPPORTED_HEAD_DIM = -2, /* D not in {64, 96, 128} */
+  NEOX_ERR_MISALIGNED = -3,           /* qkv/out not 16-byte aligned, lse not 4-byte aligned */
+  NEOX_ERR_CUDA = -4,                 /* a CUDA runtime/driver call failed (see neox_attn_last_cuda_error) */
+  NEOX_ERR_DEVICE_TIMEOUT = -5,       /* a kernel's bounded wait ran out; results are not valid */
+  NEOX_ERR_NO_DEVICE_SUPPORT = -6     /* current device is not compute capability 10.3 (B300) */
+} neox_status;
+
+/*
+ * Causal NeoX-rotary self-attention forward.
+ *
+ *   qkv          device pointer, bf16 [B, S, H, 3, D], contiguous, slot 0 = Q,
+ *                1 = K, 2 = V; 16-byte aligned; read only (never rotated in place).
+ *   B, S, H      batch, sequence length, heads; each >= 1; B*S*H*3*D < 2^40.
+ *                Any S is accepted (ragged tails are masked).
+ *   D            head dim, one of 64, 96, 128.
+ *   rotary_dim   even, 0 <= rotary_dim <= D (0 = no rotary embedding).
+ *   rotary_base  > 0 and finite (10000 for GPT-NeoX).
+ *   out          device pointer, bf16 [B, S, H, D], contiguous, 16-byte aligned;
+ *                must not overlap qkv or lse.  Written, never read.
+ *   lse          device pointer, fp32 [B, H, S], contiguous, 4-byte aligned;
+ *                natural-log logsumexp of the scaled scores of each row.
+ *   stream       a cudaStream_t (NULL = legacy default stream).
+ *
+ * Ownership: the caller owns qkv/out/lse; the library neither frees nor keeps
+ * them.  The library owns one cached fp32 cos/sin table per (device, rotary_dim,
+ * rotary_base), grown on demand; the call that builds or grows it synchronizes
+ * `stream` once, later calls do not.  neox_attn_release() frees the cache.
+ *
+ * Errors: every argument is validated before any CUDA call; on error nothing is
+ * launched and nothing is written.  NEOX_ERR_CUDA means a launch or allocation
+ * failed.  A device-side wait timeout is reported only by
+ * neox_attn_get_device_error() after the stream has been synchronized.
+ */
+int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
+                  void* out, float* lse, void* stream);
+
+/*
+ * Same contract as neox_attn_fwd, computed by the plain single-warpgroup tcgen05 kernel
+ * (one CTA per 128-row query tile, every stage in sequence).  Slower; kept as an
+ * independent second implementation of the same tile layouts for cross-checking.
+ * Limits: B <= 65535 and H <= 65535 (grid dimensions), else NEOX_ERR_INVALID_ARG.
+ */
+int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
+                         void* out, float* lse, void* stream);
+
+/*
+ * Reads and clears the current device's error word written by the kernels' bounded
+ * waits.  Call after synchronizing the streams that ran neox_attn_fwd.
+ * Returns NEOX_OK, NEOX_ERR_DEVICE_TIMEOUT, or NEOX_ERR_CUDA if the read failed.
+ */
+int neox_attn_get_device_error(void);
+
+/* A static, human-readable name for a neox_status value. */
+const char* neox_attn_status_string(int status);
+
+/* The last CUDA error code the library saw on this host thread (0 = none). */
+int neox_attn_last_cuda_error(void);
+
+/* Frees the library-owned cos/sin tables on every device.  Waits for the device
+ * first; not to be called while neox_attn_fwd work is being enqueued elsewhere. */
+void neox_attn_release(void);
+
+/*
+ * Self-test of the bounded-wait machinery: launches one tiny kernel that waits on
+ * a shared-memory barrier nothing arrives on, with a limit of `timeout_ns`
+ * nanoseconds (1e3 .. 1e9).  After the stream is synchronized,
+ * neox_attn_get_device_error() must return NEOX_ERR_DEVICE_TIMEOUT.  Nothing
+ * faults and nothing hangs; the context stays usable.
+ */
+int neox_attn_selftest_wait_timeout(int64_t timeout_ns, void* stream);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int neox_attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NEOX_ATTN_H_ */

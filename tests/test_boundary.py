@@ -1,0 +1,91 @@
+"""The C ABI without a GPU: the library loads, exports what the header declares, and
+rejects bad arguments before touching CUDA (pointers here are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import causal_rope_self_neox_b300 as na
+from causal_rope_self_neox_b300 import build as nb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "neox_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nb.build()
+    return na.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(neox_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "neox_attn_fwd" in names and "neox_attn_get_device_error" in names
+    assert set(names) == set(na.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert na.neox_attn_status_string(na.NEOX_OK) == "ok"
+    assert "head dim" in na.neox_attn_status_string(na.NEOX_ERR_UNSUPPORTED_HEAD_DIM)
+    assert na.neox_attn_status_string(12345) == "unknown status"
+    assert na.neox_attn_version() >= 100
+
+
+A = 0x10000000  # fake, 16-byte aligned device addresses: validation never dereferences them
+OUT = 0x20000000
+LSE = 0x30000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 1, 128, 2, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),          # null qkv
+    ((A, 1, 128, 2, 64, 16, 1e4, 0, LSE), na.NEOX_ERR_INVALID_ARG),            # null out
+    ((A, 1, 128, 2, 64, 16, 1e4, OUT, 0), na.NEOX_ERR_INVALID_ARG),            # null lse
+    ((A, 0, 128, 2, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),          # B = 0
+    ((A, 1, 0, 2, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),            # S = 0
+    ((A, 1, 128, 0, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),          # H = 0
+    ((A, 1, 128, 2, 80, 16, 1e4, OUT, LSE), na.NEOX_ERR_UNSUPPORTED_HEAD_DIM),  # D = 80
+    ((A, 1, 128, 2, 256, 16, 1e4, OUT, LSE), na.NEOX_ERR_UNSUPPORTED_HEAD_DIM),
+    ((A, 1, 128, 2, 64, 15, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),          # odd rotary_dim
+    ((A, 1, 128, 2, 64, 66, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),          # rotary_dim > D
+    ((A, 1, 128, 2, 64, -2, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),
+    ((A, 1, 128, 2, 64, 16, 0.0, OUT, LSE), na.NEOX_ERR_INVALID_ARG),          # base <= 0
+    ((A, 1, 128, 2, 64, 16, float("inf"), OUT, LSE), na.NEOX_ERR_INVALID_ARG),
+    ((A, 1, 128, 2, 64, 16, float("nan"), OUT, LSE), na.NEOX_ERR_INVALID_ARG),
+    ((A + 8, 1, 128, 2, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_MISALIGNED),      # qkv not 16-B aligned
+    ((A, 1, 128, 2, 64, 16, 1e4, OUT + 2, LSE), na.NEOX_ERR_MISALIGNED),
+    ((A, 1, 128, 2, 64, 16, 1e4, OUT, LSE + 2), na.NEOX_ERR_MISALIGNED),
+    ((A, 1, 128, 2, 64, 16, 1e4, A + 4096, LSE), na.NEOX_ERR_INVALID_ARG),     # out overlaps qkv
+    ((A, 1, 128, 2, 64, 16, 1e4, OUT, A + 64), na.NEOX_ERR_INVALID_ARG),       # lse overlaps qkv
+    ((A, 1 << 20, 1 << 20, 64, 128, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),  # too large
+])
+@pytest.mark.parametrize("entry", ["neox_attn_fwd", "neox_attn_fwd_simple"])
+def test_invalid_arguments_rejected_before_cuda(lib, entry, args, status):
+    fn = getattr(na, entry)
+    assert fn(*args, stream=0) == status
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU error path")
+def test_valid_arguments_without_a_gpu_report_a_cuda_error(lib):
+    rc = na.neox_attn_fwd(A, 1, 128, 2, 64, 16, 1e4, OUT, LSE, stream=0)
+    assert rc in (na.NEOX_ERR_CUDA, na.NEOX_ERR_NO_DEVICE_SUPPORT)
+    assert na.neox_attn_selftest_wait_timeout(1000, 0) in (na.NEOX_ERR_CUDA, na.NEOX_ERR_NO_DEVICE_SUPPORT)
+    assert na.neox_attn_selftest_wait_timeout(10, 0) == na.NEOX_ERR_INVALID_ARG
+
+
+def test_torch_wrapper_rejects_cpu_tensors(lib):
+    x = torch.zeros((1, 4, 1, 3, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        na.attn_fwd(x, 16)
