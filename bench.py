@@ -1,0 +1,397 @@
+#!/usr/bin/env python3
+"""Benchmark: causal NeoX-rotary self-attention forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+A step is one pass of the whole op (rotary + QK^T + causal online softmax + PV +
+epilogue, one kernel launch) over the GPT-NeoX-20B-shaped workload (B=2, H=64,
+S=2048, D=96, rotary_dim=24) unless --workload says otherwise.  Inputs are seeded,
+synthetic and already resident in HBM when the timed region starts; L2 is flushed
+(a 256 MB write) before every step, outside the per-step CUDA-event interval.
+Metric: causal FLOPs 2*B*H*S^2*D per step / kernel time, in TFLOP/s, and that figure
+as a fraction of the measured dense bf16 tensor peak.
+
+N > 1 (torchrun): every rank runs its own copy of the workload on its own seed (weak
+scaling; the op has no exchange step), the timing is the max over ranks, and the
+value is the FLOPs of all ranks over that time.
+
+--impl reference times the fp64 CPU oracle (the test oracle, as it stands) on the
+host cores on a bounded sample of the same workload per step; rank 0 only.
+One JSON line on stdout (rank 0); everything else goes to stderr.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from causal_rope_self_neox_b300.workloads import WORKLOADS, bf16_bits, make_qkv  # noqa: E402
+
+METRIC = "causal RoPE attention fwd TFLOP/s and % of B300 bf16 tensor peak"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_BF16_TFLOPS = 1800.0
+FALLBACK_HBM_GBS = 6400.0
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])), \
+            float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", "*"))) + \
+        sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.json")
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+    except Exception:
+        return None, "no ncu summary"
+    if prof.get("source_hash") != kernel_source_hash():
+        return None, "kernel changed since the ncu capture"
+    return prof.get("dram_bytes_per_launch"), path
+
+
+# ------------------------------------------------------------------ clocks ----
+class ClockSampler:
+    FIELDS = ("index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception as e:  # nvidia-smi missing: record nothing
+            log("clock sampling unavailable:", e)
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def clocks_rejected(c) -> bool:
+    if any(r in c["reasons"] for r in BAD_REASONS):
+        return True
+    if c["sm_mhz"] and c["sm_max_mhz"] and c["sm_mhz"] < 0.5 * c["sm_max_mhz"] and "sw_power_cap" not in c["reasons"]:
+        return True
+    return False
+
+
+# ------------------------------------------------------------- CPU oracle ----
+def cpu_baseline(w, qkv_cpu):
+    import oracle
+    threads = oracle.default_threads()
+    bits = bf16_bits(qkv_cpu)
+    t0 = time.perf_counter()
+    oracle.fwd(bits, w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, threads=threads)
+    dt = time.perf_counter() - t0
+    used = min(threads, w.B * w.H)
+    return {"value": w.flops / dt / 1e12, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"the whole workload ({w.B * w.H} heads x {w.S} rows), one pass, fp64, {used} threads"}
+
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step is a bounded sample of whole heads."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    threads = oracle.default_threads()
+    qkv = make_qkv(w.B, w.S, w.H, w.D, w.seed, w.k_scale)
+    bits_all = bf16_bits(qkv)
+    head_flops = 2.0 * w.S * w.S * w.D
+    # calibrate: one head on one thread
+    one = bf16_bits(qkv[:1, :, :1].contiguous())
+    t0 = time.perf_counter()
+    oracle.fwd(one, 1, w.S, 1, w.D, w.rotary_dim, w.rotary_base, threads=1)
+    per_head_1t = time.perf_counter() - t0
+    budget = 120.0
+    per_step_budget = budget / max(1, args.steps + args.warmup)
+    heads = int(max(1, min(w.B * w.H, per_step_budget / per_head_1t * threads)))
+    heads = min(heads, w.H)
+    sub = bf16_bits(qkv[:1, :, :heads].contiguous())
+    used = min(threads, heads)
+    for _ in range(args.warmup):
+        oracle.fwd(sub, 1, w.S, heads, w.D, w.rotary_dim, w.rotary_base, threads=used)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd(sub, 1, w.S, heads, w.D, w.rotary_dim, w.rotary_base, threads=used)
+        times.append(time.perf_counter() - t0)
+    flops = heads * head_flops
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    del bits_all
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "sample_heads_per_step": heads, "l2": "n/a (CPU)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+                         "sample": f"{heads} of {w.B * w.H} heads x {w.S} rows per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- rank timing ----
+def max_over_ranks(x: float, dist, device) -> float:
+    """The slowest rank's value (a timing); the identity with no process group."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (total_ms / 1e3) / 1e12
+
+
+# ------------------------------------------------------------------ GPU arm ----
+def run_ours(args, w):
+    import torch
+    import causal_rope_self_neox_b300 as na
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        log(f"note: --gpus {args.gpus} but WORLD_SIZE {world}; using WORLD_SIZE")
+    dist = None
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    qkv_cpu = make_qkv(w.B, w.S, w.H, w.D, w.seed + rank, w.k_scale)
+    qkv = qkv_cpu.to(dev)
+    out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(q=qkv):
+        rc = na.neox_attn_fwd(q.data_ptr(), w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, out.data_ptr(),
+                              lse.data_ptr(), sh)
+        if rc != 0:
+            raise na.NeoxAttnError(rc, "neox_attn_fwd")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    na.check_device_error()
+    if not bool(torch.isfinite(lse).all()):
+        raise RuntimeError("non-finite lse after warm-up")
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(local_rank)
+    try:
+        u = str(props.uuid)
+        gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+
+    def timed():
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_id) as cs:
+            t0 = time.perf_counter()
+            for i in range(args.steps):
+                flush.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+        barrier()
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return ms, wall, cs.summary()
+
+    ms, wall, clocks = timed()
+    retried = False
+    if clocks_rejected(clocks):
+        log("clock record rejected", clocks, "- measuring once more")
+        ms, wall, clocks = timed()
+        retried = True
+    na.check_device_error()
+
+    total_ms = max_over_ranks(sum(ms), dist, dev)
+    ms_per_step = total_ms / args.steps
+    value = job_tflops(w.flops, world, args.steps, total_ms)
+
+    # end to end through the public API: pinned host -> device, kernel, device -> pinned host
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    host_in = qkv_cpu.pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dev_in = torch.empty_like(qkv)
+    for _ in range(2):
+        dev_in.copy_(host_in, non_blocking=True)
+        step(dev_in)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dev_in.copy_(host_in, non_blocking=True)
+        step(dev_in)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    na.check_device_error()
+
+    if rank == 0:
+        peak, peak_sus, hbm, src = load_peaks()
+        per_gpu = w.flops / (ms_per_step / 1e3) / 1e12
+        traffic, tsrc = profiled_traffic(w.name)
+        alg_bytes = 2 * w.B * w.S * w.H * 3 * w.D + 2 * w.B * w.S * w.H * w.D + 4 * w.B * w.H * w.S
+        D = w.D
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, K x k_scale)",
+            "config": {**w.describe(), "l2": "flushed before every step (256 MB write, outside the event interval)",
+                       "parallelism": f"replicas x{world} (each rank its own workload; no collective on the data path)"},
+            "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s",
+                         "frac": per_gpu / peak, "traffic": traffic,
+                         "peak_kind": f"{src} dense bf16 burst (cuBLAS, kernel timed alone)",
+                         "frac_of_sustained": per_gpu / peak_sus,
+                         "kernel": f"attn_fwd_ws_kernel<D={D}>", "traffic_source": tsrc,
+                         "algorithmic_flops_per_launch": w.flops,
+                         "hbm_secondary": {"algorithmic_bytes_per_launch": alg_bytes,
+                                           "achieved_gbs": alg_bytes / (ms_per_step / 1e3) / 1e9,
+                                           "peak_gbs": hbm}},
+            "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+            "clocks_retried": retried,
+            "e2e": {"value": world * w.flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
+                    "d2h_bytes_per_step": host_out.numel() * host_out.element_size() + host_lse.numel() * 4,
+                    "steps": e2e_steps, "ms_per_step": e2e_ms,
+                    "path": "pinned host qkv -> device, neox_attn_fwd (C ABI), out + lse -> pinned host"},
+            "gpu_launches": args.steps,
+            "wall_s_timed_region": wall,
+            "kernel_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, qkv_cpu)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="neox20b")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -130,3 +130,17 @@ def test_output_buffers_and_rejections_on_device():
         == na.NEOX_ERR_INVALID_ARG
     assert na.neox_attn_fwd(qkv.data_ptr(), 1, 64, 1, 80, 16, 1e4, out.data_ptr(), lse.data_ptr(), s) \
         == na.NEOX_ERR_UNSUPPORTED_HEAD_DIM
+
+
+def test_head_and_batch_shards_match_the_full_call_bit_for_bit():
+    # every (batch, head) is independent: a rank owning a head range (or a batch range)
+    # computes exactly what the full call computes for it
+    B, S, H, D, r = 2, 520, 4, 96, 24
+    qkv = make_qkv(B, S, H, D, seed=31)
+    out, lse = run_gpu(qkv, r)
+    o1, l1 = run_gpu(qkv[:, :, 1:3].contiguous(), r)
+    np.testing.assert_array_equal(o1, out[:, :, 1:3])
+    np.testing.assert_array_equal(l1, lse[:, 1:3])
+    o2, l2 = run_gpu(qkv[1:].contiguous(), r)
+    np.testing.assert_array_equal(o2, out[1:])
+    np.testing.assert_array_equal(l2, lse[1:])
