@@ -22,10 +22,11 @@ NEOX_ERR_MISALIGNED = -3
 NEOX_ERR_CUDA = -4
 NEOX_ERR_DEVICE_TIMEOUT = -5
 NEOX_ERR_NO_DEVICE_SUPPORT = -6
+NEOX_ERR_TOO_LARGE = -7
 
 EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
            "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
-           "neox_attn_version")
+           "neox_attn_version", "neox_attn_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -47,7 +48,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib = ctypes.CDLL(path)
             P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
             fwd_args = [P, i32, i32, i32, i32, i32, f32, P, P, P]
-            for name in ("neox_attn_fwd", "neox_attn_fwd_simple"):
+            for name in ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_fwd_noalloc"):
                 getattr(lib, name).argtypes = fwd_args
                 getattr(lib, name).restype = i32
             lib.neox_attn_get_device_error.argtypes = []
@@ -78,6 +79,15 @@ def neox_attn_fwd_simple(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_di
                          out_ptr: int, lse_ptr: int, stream: int = 0) -> int:
     return load_library().neox_attn_fwd_simple(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr,
                                                stream)
+
+
+def neox_attn_fwd_noalloc(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
+                          out_ptr: int, lse_ptr: int, stream: int = 0) -> int:
+    """Raw call of the allocation-free variant (fixed 8 MiB cos/sin table inside the
+    library, S * rotary_dim/2 <= 1048576): for callers that cannot let the library
+    cudaMalloc.  Calls that overlap on the GPU share that table and race."""
+    return load_library().neox_attn_fwd_noalloc(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr,
+                                                stream)
 
 
 def neox_attn_get_device_error() -> int:

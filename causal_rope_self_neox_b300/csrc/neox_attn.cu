@@ -216,6 +216,31 @@ __global__ void selftest_wait_kernel(uint64_t limit_ns) {
   if (threadIdx.x == 0) neox::wait_phase(neox::smem_u32(&bar), 0, &abort_flag, limit_ns, 0xEE);
 }
 
+// ------------------------------------------------- allocation-free variant ----
+// The cos/sin table of neox_attn_fwd_noalloc lives in this fixed device array instead of
+// memory the library allocates: S * rotary_dim/2 entries at most (8 MiB).  Every GPU that
+// loads the library holds it until the process exits.  In host code the name is only a
+// host-side stand-in; the kernels get its device address from cudaGetSymbolAddress.
+constexpr int64_t kNoAllocTableEntries = int64_t(1) << 20;
+static __device__ __align__(256) float2 g_noalloc_table[kNoAllocTableEntries];
+
+std::mutex g_noalloc_mu;
+std::vector<float2*> g_noalloc_addr;  // per device ordinal; nullptr until looked up
+
+// Device address of g_noalloc_table on `device`, which must be the current device.
+int noalloc_table_address(int device, float2** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (static_cast<int>(g_noalloc_addr.size()) <= device) g_noalloc_addr.resize(device + 1, nullptr);
+  if (!g_noalloc_addr[device]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_table);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_noalloc_addr[device] = static_cast<float2*>(ptr);
+  }
+  *out = g_noalloc_addr[device];
+  return NEOX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -274,6 +299,7 @@ const char* neox_attn_status_string(int status) {
     case NEOX_ERR_CUDA: return "CUDA error";
     case NEOX_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case NEOX_ERR_NO_DEVICE_SUPPORT: return "device is not compute capability 10.3";
+    case NEOX_ERR_TOO_LARGE: return "S * rotary_dim/2 exceeds the fixed 1048576-entry table of neox_attn_fwd_noalloc";
     default: return "unknown status";
   }
 }
@@ -307,5 +333,54 @@ int neox_attn_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
 }
 
 int neox_attn_version(void) { return 100; }
+
+int neox_attn_fwd_noalloc(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out,
+                          float* lse, void* stream) {
+  try {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = validate(qkv, B, S, H, D, rotary_dim, rotary_base, out, lse);
+    if (rc != NEOX_OK) return rc;
+    if (static_cast<int64_t>(S) * (rotary_dim / 2) > kNoAllocTableEntries) return NEOX_ERR_TOO_LARGE;
+    Prepared P;
+    rc = current_device(&P.device, &P.dev);
+    if (rc != NEOX_OK) return rc;
+    float2* table = nullptr;
+    if (rotary_dim > 0) {
+      rc = noalloc_table_address(P.device, &table);
+      if (rc != NEOX_OK) return rc;
+    }
+    rc = encode_qkv_map(&P.map, qkv, B, S, H, D);
+    if (rc != NEOX_OK) return rc;
+    neox::AttnParams& p = P.p;
+    p.cs = table;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.B = B;
+    p.S = S;
+    p.H = H;
+    p.r = rotary_dim;
+    p.r16 = (rotary_dim + 15) / 16 * 16;
+    p.side_cols = rotary_dim > 0 ? (p.r16 + 31) / 32 * 32 : 0;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    p.num_units = 0;
+    p.wait_limit_ns = neox::kWaitLimitNs;
+    if (rotary_dim > 0) {
+      // rebuilt on every call, rows [0, S): the array keeps whatever the last call left
+      const int h = rotary_dim / 2;
+      const int64_t n = static_cast<int64_t>(S) * h;
+      const int blocks = static_cast<int>(std::min<int64_t>((n + 255) / 256, 65535));
+      neox::rope_table_kernel<<<blocks, 256, 0, st>>>(table, S, h, rotary_dim, static_cast<double>(rotary_base));
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    switch (D) {
+      case 64: return launch_ws<64>(P, st);
+      case 96: return launch_ws<96>(P, st);
+      default: return launch_ws<128>(P, st);
+    }
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
 
 }  // extern "C"

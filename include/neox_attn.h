@@ -44,7 +44,8 @@ typedef enum {
   NEOX_ERR_MISALIGNED = -3,           /* qkv/out not 16-byte aligned, lse not 4-byte aligned */
   NEOX_ERR_CUDA = -4,                 /* a CUDA runtime/driver call failed (see neox_attn_last_cuda_error) */
   NEOX_ERR_DEVICE_TIMEOUT = -5,       /* a kernel's bounded wait ran out; results are not valid */
-  NEOX_ERR_NO_DEVICE_SUPPORT = -6     /* current device is not compute capability 10.3 (B300) */
+  NEOX_ERR_NO_DEVICE_SUPPORT = -6,    /* current device is not compute capability 10.3 (B300) */
+  NEOX_ERR_TOO_LARGE = -7             /* neox_attn_fwd_noalloc: S * rotary_dim/2 > 1048576 */
 } neox_status;
 
 /*
@@ -84,6 +85,35 @@ int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, f
  */
 int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
                          void* out, float* lse, void* stream);
+
+/*
+ * The same computation as neox_attn_fwd, for callers that cannot let a library
+ * allocate device memory.  The pages have no counterpart to this entry point.
+ *
+ * Who needs it: a framework or inference server whose own caching allocator has
+ * already reserved nearly all of the GPU's memory (a cudaMalloc from a library would
+ * then fail, or carve a block out of memory the caller has accounted for), and
+ * request paths that must not call cudaMalloc/cudaFree at all because those calls can
+ * synchronize the device.  neox_attn_fwd allocates its cos/sin table on first use;
+ * this entry point never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Instead the cos/sin table lives in one fixed device array compiled into the library
+ * (8 MiB, 1048576 entries; every GPU that loads the library holds it until the process
+ * exits).  Limit: S * rotary_dim/2 <= 1048576 (e.g. S = 16384 with rotary_dim = 128),
+ * else NEOX_ERR_TOO_LARGE and nothing is launched.
+ *
+ * Each call rebuilds rows [0, S) of the table on `stream` and then runs the attention
+ * kernel on the same stream; the array keeps the last call's contents.  All calls share
+ * the one array, so calls that overlap on the GPU (different streams, no ordering
+ * between them) race on it and may read another call's table: order them.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ * before any stream capture.  Arguments, layouts, ownership and the other errors are
+ * those of neox_attn_fwd.
+ */
+int neox_attn_fwd_noalloc(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
+                          void* out, float* lse, void* stream);
 
 /*
  * Reads and clears the current device's error word written by the kernels' bounded
