@@ -71,16 +71,25 @@ def kernel_source_hash() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.json")
+    """DRAM bytes per launch from the committed ncu summary of this workload
+    (profiles/attn_fwd_ws_<workload>.txt, `key: value` lines), if it was taken on the
+    current kernel sources; otherwise None."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_ws_{workload}.txt")
+    prof = {}
     try:
         with open(path) as f:
-            prof = json.load(f)
-    except Exception:
+            for line in f:
+                if ":" in line and not line.startswith(("#", " ")):
+                    k, v = line.split(":", 1)
+                    prof[k.strip()] = v.strip()
+    except OSError:
         return None, "no ncu summary"
     if prof.get("source_hash") != kernel_source_hash():
         return None, "kernel changed since the ncu capture"
-    return prof.get("dram_bytes_per_launch"), path
+    try:
+        return float(prof["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
+    except (KeyError, ValueError):
+        return None, "summary without dram_bytes_per_launch"
 
 
 # ------------------------------------------------------------------ clocks ----

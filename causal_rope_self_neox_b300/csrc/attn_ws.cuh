@@ -31,6 +31,19 @@
 namespace neox {
 
 constexpr int kWsThreads = 384;
+constexpr int kRegsControl = 136;  // producer, MMA and rotary warps (warpgroup 0)
+constexpr int kRegsSoftmax = 184;  // the two softmax warpgroups
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kWsThreads * 168, "register split exceeds the launch");
+
+// Descriptor words for the 64-byte-swizzled tiles: the high word is the same for every
+// operand (SBO = 512 B, version 1, layout SW64); the low word is (address >> 4) plus
+// the leading-byte-offset field (16 B for K-major, 8 KB between 32-column blocks for V).
+constexpr uint32_t kDescHi = (512u >> 4) | (1u << 14) | (4u << 29);
+__device__ __forceinline__ uint32_t desc_lo_k(uint32_t saddr) { return (saddr >> 4) | (1u << 16); }
+__device__ __forceinline__ uint32_t desc_lo_v(uint32_t saddr) { return (saddr >> 4) | ((kBlkBytes >> 4) << 16); }
+__device__ __forceinline__ uint64_t desc_of(uint32_t lo) { return (static_cast<uint64_t>(kDescHi) << 32) | lo; }
+// Offset (in 16-byte units) of K chunk kc (16 columns) inside a column-blocked tile.
+__host__ __device__ constexpr uint32_t kchunk_off(int kc) { return (kc >> 1) * (kBlkBytes >> 4) + (kc & 1) * 2; }
 
 struct WsLayout {
   int q_raw[2], q_side[2];
@@ -93,6 +106,14 @@ __device__ __forceinline__ Unit decode_unit(int k, int B, int H, int S) {
   return u;
 }
 
+// Units in the order of decreasing work (t descending, then head), dealt to the CTAs in
+// a snake: round r covers units [rG, rG + G); even rounds go to CTAs 0..G-1, odd rounds
+// to CTAs G-1..0, which balances the longest-first list about as well as a greedy
+// dynamic scheduler would, with no atomics (so concurrent launches cannot interfere).
+__device__ __forceinline__ int snake_unit(int round, int cta, int G) {
+  return round * G + ((round & 1) ? (G - 1 - cta) : cta);
+}
+
 template <int D, int NK, int NV>
 __global__ void __launch_bounds__(kWsThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
@@ -148,9 +169,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-
+  // register split: the softmax warpgroups hold a whole 128-column S row per thread
+  // (launch: 384 x 168 = 128 x 136 + 256 x 184)
   const int G = gridDim.x;
-  if (warp == 0) {
+  if (warp < 4) {
+   regs_release<kRegsControl>();
+   if (warp == 0) {
     // ============================================================ producer ====
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
@@ -161,7 +185,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       for (int s = 0; s < NV; ++s) last_v_par[s] = -1;
       int last_q_par = -1;
       bool ok = true;
-      for (int k = blockIdx.x; k < p.num_units && ok; k += G, ++u_local) {
+      for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
+        const int k = snake_unit(rd, blockIdx.x, G);
+        if (k >= p.num_units) continue;
         const Unit u = decode_unit(k, p.B, p.H, p.S);
         if (!wait_phase(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_flag, lim, 10)) { ok = false; break; }
         const int qbytes = tile_bytes(D) * (u.n1 > 0 ? 2 : 1);
@@ -194,6 +220,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             ++vfill;
           }
         }
+        ++u_local;
       }
       if (!ok || *abort_flag) {
         // let every load this thread armed land before the CTA's shared memory goes away
@@ -209,8 +236,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       uint32_t kuse = 0, vuse = 0, u_local = 0;
       uint32_t p_cnt[2] = {0, 0};
+      const int nside = p.r16 / 16;  // 16-column chunks of lo products
       bool ok = true, issued = false;
-      for (int k = blockIdx.x; k < p.num_units && ok; k += G, ++u_local) {
+      for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
+        const int k = snake_unit(rd, blockIdx.x, G);
+        if (k >= p.num_units) continue;
         const Unit u = decode_unit(k, p.B, p.H, p.S);
         if (!wait_phase(bar(BAR_Q_READY), u_local & 1, abort_flag, lim, 30)) { ok = false; break; }
         tc_fence_after_sync();
@@ -233,21 +263,25 @@ __global__ void __launch_bounds__(kWsThreads, 1)
               if (!wait_phase(bar(BAR_P_FULL + tau), p_cnt[tau] & 1, abort_flag, lim, 33)) { ok = false; break; }
               ++p_cnt[tau];
               tc_fence_after_sync();
-              const uint32_t vaddr = smem_u32(smem + L.v[vs]);
+              const uint32_t vlo = desc_lo_v(smem_u32(smem + L.v[vs]));
 #pragma unroll
               for (int kk = 0; kk < kRows / 16; ++kk)
-                mma_ts(tO, tS + kk * 8, vmajor_desc(vaddr, kk), idesc_pv, (j > 1 || kk > 0));
+                mma_ts(tO, tS + kk * 8, desc_of(vlo + kk * 64), idesc_pv, (j > 1 || kk > 0));
               issued = true;
               if (j == n) tc_commit(bar(BAR_O_FINAL + tau));
             }
             if (j < n) {
-              const uint32_t q = smem_u32(smem + L.q_raw[tau]), qs = smem_u32(smem + L.q_side[tau]);
-              const uint32_t kr = smem_u32(smem + L.k_raw[ks]), ksd = smem_u32(smem + L.k_side[ks]);
+              const uint32_t q = desc_lo_k(smem_u32(smem + L.q_raw[tau]));
+              const uint32_t qs = desc_lo_k(smem_u32(smem + L.q_side[tau]));
+              const uint32_t kr = desc_lo_k(smem_u32(smem + L.k_raw[ks]));
+              const uint32_t ksd = desc_lo_k(smem_u32(smem + L.k_side[ks]));
 #pragma unroll
-              for (int kc = 0; kc < D / 16; ++kc) mma_ss(tS, kmajor_desc(q, kc), kmajor_desc(kr, kc), idesc_s, kc > 0);
-              for (int kc = 0; kc < p.r16 / 16; ++kc) {
-                mma_ss(tS, kmajor_desc(qs, kc), kmajor_desc(kr, kc), idesc_s, 1);
-                mma_ss(tS, kmajor_desc(q, kc), kmajor_desc(ksd, kc), idesc_s, 1);
+              for (int kc = 0; kc < D / 16; ++kc)
+                mma_ss(tS, desc_of(q + kchunk_off(kc)), desc_of(kr + kchunk_off(kc)), idesc_s, kc > 0);
+              for (int kc = 0; kc < nside; ++kc) {
+                const uint32_t o = kchunk_off(kc);
+                mma_ss(tS, desc_of(qs + o), desc_of(kr + o), idesc_s, 1);
+                mma_ss(tS, desc_of(q + o), desc_of(ksd + o), idesc_s, 1);
               }
               issued = true;
               tc_commit(bar(BAR_S_FULL + tau));
@@ -258,26 +292,36 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           if (j >= 1) { tc_commit(bar(BAR_V_EMPTY + vs)); ++vuse; }
         }
         tc_commit(bar(BAR_Q_EMPTY));
+        ++u_local;
       }
       if (issued && (!ok || *abort_flag)) {
         tc_commit(bar(BAR_DRAIN));
         drain_phase(bar(BAR_DRAIN), 0, lim);
       }
     }
-  } else if (warp < 4) {
+   } else {
     // ======================================================= rotary transform ====
     const int tt = tid - 64;  // 0..63: rows tt and tt + 64
+    const int h = p.r >> 1;
+    const bool staged = p.r > 0 && (h & 1) == 0 && h <= kCsChunkPairs;  // whole row in one chunk
+    auto kpos = [&](int j, int row) -> int64_t {
+      const int64_t pos = static_cast<int64_t>(j) * kRows + row;
+      return pos < p.S ? pos : -1;
+    };
     uint32_t kuse = 0, u_local = 0;
-    for (int k = blockIdx.x; k < p.num_units; k += G, ++u_local) {
+    CsChunk next;  // table entries of the next K block, loaded ahead of its data
+    for (int rd = 0; rd * G < p.num_units; ++rd) {
+      const int k = snake_unit(rd, blockIdx.x, G);
+      if (k >= p.num_units) continue;
       const Unit u = decode_unit(k, p.B, p.H, p.S);
+      if (staged) cs_load(next, p.cs, h, 0, kpos(0, tt), kpos(0, tt + 64));
       if (!wait_phase(bar(BAR_Q_FULL), u_local & 1, abort_flag, lim, 20)) break;
       if (p.r > 0) {
-        for (int t = 0; t < (u.n1 > 0 ? 2 : 1); ++t)
-          for (int rr = 0; rr < 2; ++rr) {
-            const int row = tt + rr * 64;
-            const int64_t pos = static_cast<int64_t>(2 * u.t + t) * kRows + row;
-            rotate_row(smem + L.q_raw[t], smem + L.q_side[t], row, pos < p.S ? pos : -1, p.cs, p.r);
-          }
+        for (int t = 0; t < (u.n1 > 0 ? 2 : 1); ++t) {
+          const int qt = 2 * u.t + t;
+          rotate_two_rows(smem + L.q_raw[t], smem + L.q_side[t], tt, tt + 64, kpos(qt, tt), kpos(qt, tt + 64), p.cs,
+                          p.r);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(BAR_Q_READY));
@@ -285,20 +329,23 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       for (int j = 0; j < u.nkv; ++j) {
         const int s = kuse % NK;
         if (!wait_phase(bar(BAR_K_FULL + s), (kuse / NK) & 1, abort_flag, lim, 21)) { ok = false; break; }
-        if (p.r > 0) {
-          for (int rr = 0; rr < 2; ++rr) {
-            const int row = tt + rr * 64;
-            const int64_t pos = static_cast<int64_t>(j) * kRows + row;
-            rotate_row(smem + L.k_raw[s], smem + L.k_side[s], row, pos < p.S ? pos : -1, p.cs, p.r);
-          }
+        if (staged) {
+          rotate_chunk(smem + L.k_raw[s], smem + L.k_side[s], tt, h, 0, next.v[0]);
+          rotate_chunk(smem + L.k_raw[s], smem + L.k_side[s], tt + 64, h, 0, next.v[1]);
+        } else if (p.r > 0) {
+          rotate_two_rows(smem + L.k_raw[s], smem + L.k_side[s], tt, tt + 64, kpos(j, tt), kpos(j, tt + 64), p.cs, p.r);
         }
         fence_proxy_async_smem();
         mbar_arrive(bar(BAR_K_READY + s));
         ++kuse;
+        if (staged && j + 1 < u.nkv) cs_load(next, p.cs, h, 0, kpos(j + 1, tt), kpos(j + 1, tt + 64));
       }
       if (!ok) break;
+      ++u_local;
     }
+   }
   } else {
+    regs_acquire<kRegsSoftmax>();
     // ========================================== softmax / correction / epilogue ====
     const int tau = (warp - 4) >> 2;          // query tile of this warpgroup
     const int row = tid - 128 * (tau + 1);     // 0..127: this thread's row / TMEM lane
@@ -306,7 +353,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t tS = tmem + tau * 128 + lane_off, tO = tmem + 256 + tau * 128 + lane_off;
     const float sl2 = p.scale_log2;
     uint32_t s_use = 0, o_use = 0;
-    for (int k = blockIdx.x; k < p.num_units; k += G) {
+    for (int rd = 0; rd * G < p.num_units; ++rd) {
+      const int k = snake_unit(rd, blockIdx.x, G);
+      if (k >= p.num_units) continue;
       const Unit u = decode_unit(k, p.B, p.H, p.S);
       const int n = tau == 0 ? u.n0 : u.n1;
       if (n == 0) continue;
@@ -326,9 +375,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c > row) sr[c] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row max: eight independent chains of 3-input max over 16 columns each
+        float mc[8];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t* v = sr + 16 * g;
+          float m = fmax3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+          for (int q = 3; q < 15; q += 2) m = fmax3f(m, __uint_as_float(v[q]), __uint_as_float(v[q + 1]));
+          mc[g] = fmaxf(m, __uint_as_float(v[15]));
+        }
+        const float mx = fmaxf(fmax3f(mc[0], mc[1], mc[2]), fmax3f(fmax3f(mc[3], mc[4], mc[5]), mc[6], mc[7]));
         const float mx_s = mx * sl2;
         float m_new = m_used;
         bool rescale = false;
@@ -339,15 +396,23 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           rescale = true;
         }
         const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.0f;
-        float rowsum = 0.0f;
+        // p = 2^(s * log2(e)/sqrt(D) - m): packed fp32 FMA, MUFU exp2, four packed partial sums
+        const uint64_t sc2 = f32x2_pack(sl2, sl2), nm2 = f32x2_pack(-m_new, -m_new);
+        uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -m_new));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -m_new));
-          rowsum += p0 + p1;
+          const uint64_t t = ffma2(f32x2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, nm2);
+          float t0, t1;
+          f32x2_unpack(t, t0, t1);
+          const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+          acc[c & 3] = fadd2(acc[c & 3], f32x2_pack(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
+        acc[0] = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+        float rs0, rs1;
+        f32x2_unpack(acc[0], rs0, rs1);
+        const float rowsum = rs0 + rs1;
         l_run = l_run * alpha + rowsum;
         m_used = m_new;
         // lazy correction: O holds sum over blocks < j (landed, see s_full); rescale it only

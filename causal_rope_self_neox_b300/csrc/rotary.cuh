@@ -95,4 +95,76 @@ __device__ __forceinline__ void rotate_row(uint8_t* tile, uint8_t* side, int row
   }
 }
 
+// ---- register-staged variant: the table loads of a whole chunk are issued together
+// (and can be issued ahead of the shared-memory data), so a row costs one L2 round trip
+// per chunk of pairs instead of one per pair.  Needs r/2 even (float4 = two pairs).
+constexpr int kCsChunkPairs = 12;
+
+struct CsChunk {
+  float4 v[2][kCsChunkPairs / 2];  // two rows x (cos_i, sin_i, cos_i+1, sin_i+1) per pair of pairs
+};
+
+// Table entries for pairs [i0, i0 + kCsChunkPairs) of two rows at positions p0, p1 (< 0: past the
+// end of the sequence, loaded as the identity rotation).
+__device__ __forceinline__ void cs_load(CsChunk& c, const float2* __restrict__ cs, int h, int i0, int64_t p0,
+                                        int64_t p1) {
+#pragma unroll
+  for (int q = 0; q < kCsChunkPairs / 2; ++q) {
+    const int i = i0 + 2 * q;
+    float4 a = make_float4(1.0f, 0.0f, 1.0f, 0.0f), b = a;
+    if (i < h) {
+      if (p0 >= 0) a = __ldg(reinterpret_cast<const float4*>(cs + p0 * h + i));
+      if (p1 >= 0) b = __ldg(reinterpret_cast<const float4*>(cs + p1 * h + i));
+    }
+    c.v[0][q] = a;
+    c.v[1][q] = b;
+  }
+}
+
+// Rotate pairs [i0, i0 + kCsChunkPairs) of one row with table entries already in registers.
+__device__ __forceinline__ void rotate_chunk(uint8_t* __restrict__ tile, uint8_t* __restrict__ side, int row, int h,
+                                             int i0, const float4 (&t)[kCsChunkPairs / 2]) {
+#pragma unroll
+  for (int q = 0; q < kCsChunkPairs / 2; ++q) {
+    const int i = i0 + 2 * q;
+    if (i >= h) break;
+    uint32_t* pa = reinterpret_cast<uint32_t*>(tile + sw64_off(row, i));
+    uint32_t* pb = reinterpret_cast<uint32_t*>(tile + sw64_off(row, i + h));
+    const uint32_t a = *pa, b = *pb;
+    const float x0 = bf16_bits_to_f32(static_cast<uint16_t>(a & 0xFFFF));
+    const float x1 = bf16_bits_to_f32(static_cast<uint16_t>(a >> 16));
+    const float z0 = bf16_bits_to_f32(static_cast<uint16_t>(b & 0xFFFF));
+    const float z1 = bf16_bits_to_f32(static_cast<uint16_t>(b >> 16));
+    const float y0 = fmaf(x0, t[q].x, -z0 * t[q].y), w0 = fmaf(z0, t[q].x, x0 * t[q].y);
+    const float y1 = fmaf(x1, t[q].z, -z1 * t[q].w), w1 = fmaf(z1, t[q].z, x1 * t[q].w);
+    uint16_t hy0, ly0, hy1, ly1, hw0, lw0, hw1, lw1;
+    split_hi_lo(y0, hy0, ly0);
+    split_hi_lo(y1, hy1, ly1);
+    split_hi_lo(w0, hw0, lw0);
+    split_hi_lo(w1, hw1, lw1);
+    *pa = static_cast<uint32_t>(hy0) | (static_cast<uint32_t>(hy1) << 16);
+    *pb = static_cast<uint32_t>(hw0) | (static_cast<uint32_t>(hw1) << 16);
+    *reinterpret_cast<uint32_t*>(side + sw64_off(row, i)) = static_cast<uint32_t>(ly0) | (static_cast<uint32_t>(ly1) << 16);
+    *reinterpret_cast<uint32_t*>(side + sw64_off(row, i + h)) =
+        static_cast<uint32_t>(lw0) | (static_cast<uint32_t>(lw1) << 16);
+  }
+}
+
+// Two rows of a tile, every chunk: loads of a chunk in flight together.
+__device__ __forceinline__ void rotate_two_rows(uint8_t* tile, uint8_t* side, int row0, int row1, int64_t p0,
+                                                int64_t p1, const float2* __restrict__ cs, int r) {
+  const int h = r >> 1;
+  if ((h & 1) == 0) {
+    for (int i0 = 0; i0 < h; i0 += kCsChunkPairs) {
+      CsChunk c;
+      cs_load(c, cs, h, i0, p0, p1);
+      rotate_chunk(tile, side, row0, h, i0, c.v[0]);
+      rotate_chunk(tile, side, row1, h, i0, c.v[1]);
+    }
+  } else {
+    rotate_row(tile, side, row0, p0, cs, r);
+    rotate_row(tile, side, row1, p1, cs, r);
+  }
+}
+
 }  // namespace neox
