@@ -303,42 +303,65 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // ======================================================= rotary transform ====
     const int tt = tid - 64;  // 0..63: rows tt and tt + 64
     const int h = p.r >> 1;
-    const bool staged = p.r > 0 && (h & 1) == 0 && h <= kCsChunkPairs;  // whole row in one chunk
+    // 0: no rotary.  With the table of the next tile loaded one K block ahead:
+    // 1: r = 8, 3: r = 24 (whole rotated prefix in registers), 2: r = 16, 4: r = 32
+    // (groups of 8 pairs).  5: r % 16 == 0 and r > 32, groups with their table loads
+    // double-buffered inside the tile.  6: anything else, the scalar path.
+    int kind = 0;
+    if (p.r > 0) kind = (p.r % 8 == 0 && p.r <= 32) ? p.r / 8 : ((p.r % 16 == 0) ? 5 : 6);
     auto kpos = [&](int j, int row) -> int64_t {
       const int64_t pos = static_cast<int64_t>(j) * kRows + row;
       return pos < p.S ? pos : -1;
     };
+    float4 tn0[8], tn1[8];  // table entries of rows tt, tt + 64 of the next tile (kinds 1..4)
+    auto prefetch = [&](int64_t p0, int64_t p1) {
+      switch (kind) {
+        case 1: cs_load_n<2>(tn0, p.cs, h, 0, p0); cs_load_n<2>(tn1, p.cs, h, 0, p1); break;
+        case 2: cs_load_n<4>(tn0, p.cs, h, 0, p0); cs_load_n<4>(tn1, p.cs, h, 0, p1); break;
+        case 3: cs_load_n<6>(tn0, p.cs, h, 0, p0); cs_load_n<6>(tn1, p.cs, h, 0, p1); break;
+        case 4: cs_load_n<8>(tn0, p.cs, h, 0, p0); cs_load_n<8>(tn1, p.cs, h, 0, p1); break;
+        default: break;
+      }
+    };
+    auto rotate = [&](uint8_t* tile, uint8_t* side, int64_t p0, int64_t p1) {
+      switch (kind) {
+        case 1: rotate_row_small<1>(tile, side, tt, tn0); rotate_row_small<1>(tile, side, tt + 64, tn1); break;
+        case 3: rotate_row_small<3>(tile, side, tt, tn0); rotate_row_small<3>(tile, side, tt + 64, tn1); break;
+        case 4:
+          rotate_group8(tile, side, tt, 8, h, tn0 + 4);
+          rotate_group8(tile, side, tt + 64, 8, h, tn1 + 4);  // fallthrough to group 0
+        case 2:
+          rotate_group8(tile, side, tt, 0, h, tn0);
+          rotate_group8(tile, side, tt + 64, 0, h, tn1);
+          break;
+        case 5: rotate_two_rows_groups(tile, side, tt, tt + 64, p0, p1, p.cs, h, tn0, tn1); break;
+        case 6: rotate_row(tile, side, tt, p0, p.cs, p.r); rotate_row(tile, side, tt + 64, p1, p.cs, p.r); break;
+        default: break;
+      }
+    };
     uint32_t kuse = 0, u_local = 0;
-    CsChunk next;  // table entries of the next K block, loaded ahead of its data
     for (int rd = 0; rd * G < p.num_units; ++rd) {
       const int k = snake_unit(rd, blockIdx.x, G);
       if (k >= p.num_units) continue;
       const Unit u = decode_unit(k, p.B, p.H, p.S);
-      if (staged) cs_load(next, p.cs, h, 0, kpos(0, tt), kpos(0, tt + 64));
       if (!wait_phase(bar(BAR_Q_FULL), u_local & 1, abort_flag, lim, 20)) break;
-      if (p.r > 0) {
-        for (int t = 0; t < (u.n1 > 0 ? 2 : 1); ++t) {
-          const int qt = 2 * u.t + t;
-          rotate_two_rows(smem + L.q_raw[t], smem + L.q_side[t], tt, tt + 64, kpos(qt, tt), kpos(qt, tt + 64), p.cs,
-                          p.r);
-        }
+      for (int t = 0; t < (u.n1 > 0 ? 2 : 1) && kind > 0; ++t) {
+        const int qt = 2 * u.t + t;
+        prefetch(kpos(qt, tt), kpos(qt, tt + 64));
+        rotate(smem + L.q_raw[t], smem + L.q_side[t], kpos(qt, tt), kpos(qt, tt + 64));
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(BAR_Q_READY));
+      prefetch(kpos(0, tt), kpos(0, tt + 64));
       bool ok = true;
       for (int j = 0; j < u.nkv; ++j) {
         const int s = kuse % NK;
         if (!wait_phase(bar(BAR_K_FULL + s), (kuse / NK) & 1, abort_flag, lim, 21)) { ok = false; break; }
-        if (staged) {
-          rotate_chunk(smem + L.k_raw[s], smem + L.k_side[s], tt, h, 0, next.v[0]);
-          rotate_chunk(smem + L.k_raw[s], smem + L.k_side[s], tt + 64, h, 0, next.v[1]);
-        } else if (p.r > 0) {
-          rotate_two_rows(smem + L.k_raw[s], smem + L.k_side[s], tt, tt + 64, kpos(j, tt), kpos(j, tt + 64), p.cs, p.r);
-        }
+        rotate(smem + L.k_raw[s], smem + L.k_side[s], kpos(j, tt), kpos(j, tt + 64));
         fence_proxy_async_smem();
         mbar_arrive(bar(BAR_K_READY + s));
         ++kuse;
-        if (staged && j + 1 < u.nkv) cs_load(next, p.cs, h, 0, kpos(j + 1, tt), kpos(j + 1, tt + 64));
+        if (j + 1 < u.nkv) prefetch(kpos(j + 1, tt), kpos(j + 1, tt + 64));
       }
       if (!ok) break;
       ++u_local;

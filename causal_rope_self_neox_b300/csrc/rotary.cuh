@@ -167,4 +167,110 @@ __device__ __forceinline__ void rotate_two_rows(uint8_t* tile, uint8_t* side, in
   }
 }
 
+// ---- vectorised variants: whole 16-byte chunks (8 dims) per shared access --------
+// bf16x8 <-> fp32 helpers
+__device__ __forceinline__ void unpack8(const uint4 v, float* x) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(w[k] << 16);
+    x[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+// hi = bf16(y), lo = bf16(y - hi) for 8 values, packed
+__device__ __forceinline__ void split8(const float* y, uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    h[k] = pack_bf16x2(y[2 * k], y[2 * k + 1]);
+    const float r0 = y[2 * k] - __uint_as_float(h[k] << 16);
+    const float r1 = y[2 * k + 1] - __uint_as_float(h[k] & 0xFFFF0000u);
+    l[k] = pack_bf16x2(r0, r1);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Table entries of pairs [i0, i0 + 2n) of a row at position pos (< 0: identity), as n
+// float4 = (cos_i, sin_i, cos_i+1, sin_i+1).  Needs r/2 and i0 even.
+template <int N>
+__device__ __forceinline__ void cs_load_n(float4* t, const float2* __restrict__ cs, int h, int i0, int64_t pos) {
+#pragma unroll
+  for (int q = 0; q < N; ++q)
+    t[q] = pos >= 0 ? __ldg(reinterpret_cast<const float4*>(cs + pos * h + i0 + 2 * q)) : make_float4(1.f, 0.f, 1.f, 0.f);
+}
+
+// r = 8 * NCH <= 32: the whole rotated prefix of the row lives in registers; NCH chunk
+// loads, then NCH hi stores (in place) and NCH lo stores (side tile).
+template <int NCH>
+__device__ __forceinline__ void rotate_row_small(uint8_t* __restrict__ tile, uint8_t* __restrict__ side, int row,
+                                                 const float4* t) {
+  constexpr int R = 8 * NCH, HH = R / 2;
+  float x[R], y[R];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, 8 * c)), x + 8 * c);
+#pragma unroll
+  for (int i = 0; i < HH; ++i) {
+    const float cth = (i & 1) ? t[i >> 1].z : t[i >> 1].x;
+    const float sth = (i & 1) ? t[i >> 1].w : t[i >> 1].y;
+    y[i] = fmaf(x[i], cth, -x[i + HH] * sth);
+    y[i + HH] = fmaf(x[i + HH], cth, x[i] * sth);
+  }
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    uint4 hi, lo;
+    split8(y + 8 * c, hi, lo);
+    *reinterpret_cast<uint4*>(tile + sw64_off(row, 8 * c)) = hi;
+    *reinterpret_cast<uint4*>(side + sw64_off(row, 8 * c)) = lo;
+  }
+}
+
+// r % 16 == 0: eight pairs (i0..i0+7 with partners i0+h..i0+h+7) per step, two chunks
+// in, four chunks out.
+__device__ __forceinline__ void rotate_group8(uint8_t* __restrict__ tile, uint8_t* __restrict__ side, int row, int i0,
+                                              int h, const float4* t) {
+  float x[8], z[8], y[8], w[8];
+  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0)), x);
+  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0 + h)), z);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float cth = (i & 1) ? t[i >> 1].z : t[i >> 1].x;
+    const float sth = (i & 1) ? t[i >> 1].w : t[i >> 1].y;
+    y[i] = fmaf(x[i], cth, -z[i] * sth);
+    w[i] = fmaf(z[i], cth, x[i] * sth);
+  }
+  uint4 hi, lo;
+  split8(y, hi, lo);
+  *reinterpret_cast<uint4*>(tile + sw64_off(row, i0)) = hi;
+  *reinterpret_cast<uint4*>(side + sw64_off(row, i0)) = lo;
+  split8(w, hi, lo);
+  *reinterpret_cast<uint4*>(tile + sw64_off(row, i0 + h)) = hi;
+  *reinterpret_cast<uint4*>(side + sw64_off(row, i0 + h)) = lo;
+}
+
+// Two rows of a tile for r % 16 == 0, any size: group g's table loads are issued while
+// group g-1 is being rotated.  t0 / t1 (8 float4 each) are the caller's buffers for
+// rows row0 / row1: entries [0, 4) and [4, 8) alternate between groups.
+__device__ __forceinline__ void rotate_two_rows_groups(uint8_t* tile, uint8_t* side, int row0, int row1, int64_t p0,
+                                                       int64_t p1, const float2* __restrict__ cs, int h, float4* t0,
+                                                       float4* t1) {
+  cs_load_n<4>(t0, cs, h, 0, p0);
+  cs_load_n<4>(t1, cs, h, 0, p1);
+  for (int i0 = 0; i0 < h; i0 += 16) {
+    if (i0 + 8 < h) {
+      cs_load_n<4>(t0 + 4, cs, h, i0 + 8, p0);
+      cs_load_n<4>(t1 + 4, cs, h, i0 + 8, p1);
+    }
+    rotate_group8(tile, side, row0, i0, h, t0);
+    rotate_group8(tile, side, row1, i0, h, t1);
+    if (i0 + 8 >= h) break;
+    if (i0 + 16 < h) {
+      cs_load_n<4>(t0, cs, h, i0 + 16, p0);
+      cs_load_n<4>(t1, cs, h, i0 + 16, p1);
+    }
+    rotate_group8(tile, side, row0, i0 + 8, h, t0 + 4);
+    rotate_group8(tile, side, row1, i0 + 8, h, t1 + 4);
+  }
+}
+
 }  // namespace neox
