@@ -28,6 +28,7 @@ struct AttnParams {
   int side_cols;       // r16 rounded up to a multiple of 32 (side tile width), 0 if r == 0
   float scale_log2;    // log2(e) / sqrt(D)
   int num_units;       // work units (persistent kernel)
+  int nk, nv;          // K and V ring depths (1..4), set at launch from the shared-memory budget
   uint64_t wait_limit_ns;
 };
 
@@ -35,10 +36,36 @@ __device__ __forceinline__ void record_error(unsigned int code, unsigned int sit
   atomicOr(&g_device_error, code | (site << 8));
 }
 
-// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting or the limit ran
-// out (then the abort flag is raised and the error recorded).
+// Bounded wait on an mbarrier phase, slow path: polls until the phase completes, the CTA
+// aborts, or the limit runs out (then the abort flag is raised and the error recorded).
+// Kept out of line so the many wait sites do not each carry a copy.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             uint64_t limit_ns, unsigned int site) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      record_error(kErrTimeout, site);
+      return false;
+    }
+  }
+}
+
+// Returns false if the CTA is aborting or the limit ran out.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit_ns,
                                            unsigned int site) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort_flag, limit_ns, site);
+}
+
+// The same wait fully inline, for code running with a raised register count (setmaxnreg),
+// where ptxas cannot place a call.
+__device__ __forceinline__ bool wait_phase_inline(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns, unsigned int site) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {

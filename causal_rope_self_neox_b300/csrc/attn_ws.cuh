@@ -2,7 +2,7 @@
 //
 // One CTA per SM (persistent).  A work unit is (b, h, t): the two 128-row query tiles
 // 2t and 2t+1 of one head, which share one stream of 128-key K/V blocks.  Units are
-// taken longest first (descending t) in a static stride over the CTAs.
+// taken longest first (descending t), dealt to the CTAs in a snake order.
 //
 // Roles (384 threads):
 //   warp 0        TMA producer: Q tiles once per unit, then K_j / V_j into rings
@@ -24,6 +24,10 @@
 // PV_tau(j-1) has landed: the softmax may rescale O_tau in place right then.
 //
 // Causality: tile q visits KV blocks 0..q only, and masks keys > row on block q.
+//
+// Code size matters here: every role shares the SM's instruction caches, so the
+// rotation variant is a template parameter (one path per kernel) and each role has a
+// single copy of its inner loop.
 #pragma once
 
 #include "attn_common.cuh"
@@ -34,6 +38,7 @@ constexpr int kWsThreads = 384;
 constexpr int kRegsControl = 136;  // producer, MMA and rotary warps (warpgroup 0)
 constexpr int kRegsSoftmax = 184;  // the two softmax warpgroups
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kWsThreads * 168, "register split exceeds the launch");
+constexpr int kMaxRing = 4;
 
 // Descriptor words for the 64-byte-swizzled tiles: the high word is the same for every
 // operand (SBO = 512 B, version 1, layout SW64); the low word is (address >> 4) plus
@@ -45,10 +50,22 @@ __device__ __forceinline__ uint64_t desc_of(uint32_t lo) { return (static_cast<u
 // Offset (in 16-byte units) of K chunk kc (16 columns) inside a column-blocked tile.
 __host__ __device__ constexpr uint32_t kchunk_off(int kc) { return (kc >> 1) * (kBlkBytes >> 4) + (kc & 1) * 2; }
 
+// How the rotary warps rotate a row (fixed per kernel instance):
+//   kRotNone: no rotary dims.  kRotR16 / kRotR32: r = 16 / 32, groups of 8 pairs with the
+//   next tile's table entries loaded ahead.  kRotR24: r = 24, the 24-dim prefix in
+//   registers, table loaded ahead.  kRotGroups: r % 16 == 0 and r > 32, groups of 8 pairs
+//   with double-buffered table loads inside the tile.  kRotScalar: any other even r.
+enum : int { kRotNone = 0, kRotR16 = 1, kRotR24 = 2, kRotR32 = 3, kRotGroups = 4, kRotScalar = 5 };
+__host__ __device__ constexpr int rot_kind(int r) {
+  return r == 0 ? kRotNone : r == 16 ? kRotR16 : r == 24 ? kRotR24 : r == 32 ? kRotR32 : (r % 16 == 0 ? kRotGroups : kRotScalar);
+}
+// float4 table entries per row loaded ahead of a tile's data.
+__host__ __device__ constexpr int rot_ahead(int rk) { return rk == kRotR16 ? 4 : rk == kRotR24 ? 6 : rk == kRotR32 ? 8 : 0; }
+
 struct WsLayout {
   int q_raw[2], q_side[2];
-  int k_raw[4], k_side[4];
-  int v[4];
+  int k_raw[kMaxRing], k_side[kMaxRing];
+  int v[kMaxRing];
   int bars;
   int total;
 };
@@ -83,7 +100,8 @@ enum : int {
   BAR_K_EMPTY = 18, // +slot
   BAR_V_FULL = 22,  // +slot (4)
   BAR_V_EMPTY = 26, // +slot
-  BAR_COUNT = 30
+  BAR_Q_READY1 = 30,  // query tile 1 rotated (BAR_Q_READY: tile 0)
+  BAR_COUNT = 31
 };
 
 struct Unit {
@@ -114,11 +132,12 @@ __device__ __forceinline__ int snake_unit(int round, int cta, int G) {
   return round * G + ((round & 1) ? (G - 1 - cta) : cta);
 }
 
-template <int D, int NK, int NV>
+template <int D, int RK>
 __global__ void __launch_bounds__(kWsThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int NK = p.nk, NV = p.nv;
   const WsLayout L = ws_layout(D, p.side_cols, NK, NV);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
@@ -132,6 +151,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   if (tid == 0) {
     mbar_init(bar(BAR_Q_FULL), 1);
     mbar_init(bar(BAR_Q_READY), 64);
+    mbar_init(bar(BAR_Q_READY1), 64);
     mbar_init(bar(BAR_Q_EMPTY), 1);
     mbar_init(bar(BAR_DRAIN), 1);
     for (int t = 0; t < 2; ++t) {
@@ -157,7 +177,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     tmem_relinquish();
   }
   // side tiles start at zero; columns >= r are never written again
-  if (p.side_cols > 0) {
+  if (RK != kRotNone) {
     const int sb = tile_bytes(p.side_cols);
     for (int i = tid * 16; i < sb; i += kWsThreads * 16) {
       for (int t = 0; t < 2; ++t) *reinterpret_cast<uint4*>(smem + L.q_side[t] + i) = make_uint4(0, 0, 0, 0);
@@ -171,6 +191,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // register split: the softmax warpgroups hold a whole 128-column S row per thread
   // (launch: 384 x 168 = 128 x 136 + 256 x 184)
+
   const int G = gridDim.x;
   if (warp < 4) {
    regs_release<kRegsControl>();
@@ -179,10 +200,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
       const uint64_t pol_q = l2_policy_evict_first();
-      uint32_t kfill = 0, vfill = 0, u_local = 0;
-      int last_k_par[NK], last_v_par[NV];
-      for (int s = 0; s < NK; ++s) last_k_par[s] = -1;
-      for (int s = 0; s < NV; ++s) last_v_par[s] = -1;
+      int ks = 0, vs = 0;        // next K / V ring slot
+      uint32_t kph = 0, vph = 0;  // ring lap parity of that slot
+      uint32_t u_local = 0;
+      // for the abort path: which ring slots have a load armed, and its phase parity
+      uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
       int last_q_par = -1;
       bool ok = true;
       for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
@@ -190,34 +212,38 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (k >= p.num_units) continue;
         const Unit u = decode_unit(k, p.B, p.H, p.S);
         if (!wait_phase(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_flag, lim, 10)) { ok = false; break; }
-        const int qbytes = tile_bytes(D) * (u.n1 > 0 ? 2 : 1);
-        mbar_arrive_expect_tx(bar(BAR_Q_FULL), qbytes);
+        const int nq = u.n1 > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(bar(BAR_Q_FULL), tile_bytes(D) * nq);
         last_q_par = u_local & 1;
-        for (int t = 0; t < (u.n1 > 0 ? 2 : 1); ++t)
+        for (int t = 0; t < nq; ++t)
           for (int cb = 0; cb < D / kBlkCols; ++cb)
             tma_load_4d_hint(smem_u32(smem + L.q_raw[t] + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
                              3 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
         // K_j before V_{j-1}: the order in which the MMA warp consumes them
         for (int j = 0; j <= u.nkv && ok; ++j) {
           if (j < u.nkv) {
-            const int s = kfill % NK;
-            if (!wait_phase(bar(BAR_K_EMPTY + s), ((kfill / NK) & 1) ^ 1, abort_flag, lim, 11)) { ok = false; break; }
+            const int s = ks;
+            const uint32_t par = kph;
+            if (!wait_phase(bar(BAR_K_EMPTY + s), par ^ 1, abort_flag, lim, 11)) { ok = false; break; }
             mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D));
-            last_k_par[s] = (kfill / NK) & 1;
+            k_armed |= 1u << s;
+            k_par = (k_par & ~(1u << s)) | (par << s);
             for (int cb = 0; cb < D / kBlkCols; ++cb)
               tma_load_4d_hint(smem_u32(smem + L.k_raw[s] + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s),
                                cb * kBlkCols, 3 * u.h + 1, j * kRows, u.b, pol_kv);
-            ++kfill;
+            if (++ks == NK) { ks = 0; kph ^= 1; }
           }
           if (j >= 1) {
-            const int s = vfill % NV;
-            if (!wait_phase(bar(BAR_V_EMPTY + s), ((vfill / NV) & 1) ^ 1, abort_flag, lim, 12)) { ok = false; break; }
+            const int s = vs;
+            const uint32_t par = vph;
+            if (!wait_phase(bar(BAR_V_EMPTY + s), par ^ 1, abort_flag, lim, 12)) { ok = false; break; }
             mbar_arrive_expect_tx(bar(BAR_V_FULL + s), tile_bytes(D));
-            last_v_par[s] = (vfill / NV) & 1;
+            v_armed |= 1u << s;
+            v_par = (v_par & ~(1u << s)) | (par << s);
             for (int cb = 0; cb < D / kBlkCols; ++cb)
               tma_load_4d_hint(smem_u32(smem + L.v[s] + cb * kBlkBytes), &tmap, bar(BAR_V_FULL + s), cb * kBlkCols,
                                3 * u.h + 2, (j - 1) * kRows, u.b, pol_kv);
-            ++vfill;
+            if (++vs == NV) { vs = 0; vph ^= 1; }
           }
         }
         ++u_local;
@@ -225,36 +251,45 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (!ok || *abort_flag) {
         // let every load this thread armed land before the CTA's shared memory goes away
         if (last_q_par >= 0) drain_phase(bar(BAR_Q_FULL), last_q_par, lim);
-        for (int s = 0; s < NK; ++s) if (last_k_par[s] >= 0) drain_phase(bar(BAR_K_FULL + s), last_k_par[s], lim);
-        for (int s = 0; s < NV; ++s) if (last_v_par[s] >= 0) drain_phase(bar(BAR_V_FULL + s), last_v_par[s], lim);
+        for (int s = 0; s < NK; ++s)
+          if (k_armed & (1u << s)) drain_phase(bar(BAR_K_FULL + s), (k_par >> s) & 1, lim);
+        for (int s = 0; s < NV; ++s)
+          if (v_armed & (1u << s)) drain_phase(bar(BAR_V_FULL + s), (v_par >> s) & 1, lim);
       }
     }
-  } else if (warp == 1) {
+   } else if (warp == 1) {
     // ============================================================ MMA issuer ====
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
-      uint32_t kuse = 0, vuse = 0, u_local = 0;
+      // Every operand buffer sits at a fixed shared address for the whole kernel, so each
+      // descriptor is a base below plus a constant: the issue loop is adds and MMAs only.
+      const uint64_t dq[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_raw[0]))),
+                              desc_of(desc_lo_k(smem_u32(smem + L.q_raw[1])))};
+      const uint64_t dqs[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_side[0]))),
+                               desc_of(desc_lo_k(smem_u32(smem + L.q_side[1])))};
+      const uint64_t dk0 = desc_of(desc_lo_k(smem_u32(smem + L.k_raw[0])));
+      const uint64_t dks0 = desc_of(desc_lo_k(smem_u32(smem + L.k_side[0])));
+      const uint64_t dv0 = desc_of(desc_lo_v(smem_u32(smem + L.v[0])));
+      const uint32_t kstep = static_cast<uint32_t>(tile_bytes(D) + tile_bytes(p.side_cols)) >> 4;
+      const uint32_t vstep = static_cast<uint32_t>(tile_bytes(D)) >> 4;
+      int kslot = 0, vslot = 0;
+      uint32_t kph = 0, vph = 0, u_local = 0;
       uint32_t p_cnt[2] = {0, 0};
-      const int nside = p.r16 / 16;  // 16-column chunks of lo products
+      uint32_t q1_cnt = 0;  // units with a query tile 1 (a ragged last block may have none)
+      const int nside = p.r16 / 16;  // 16-column chunks of lo products (<= 8)
       bool ok = true, issued = false;
       for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
         const int k = snake_unit(rd, blockIdx.x, G);
         if (k >= p.num_units) continue;
         const Unit u = decode_unit(k, p.B, p.H, p.S);
-        if (!wait_phase(bar(BAR_Q_READY), u_local & 1, abort_flag, lim, 30)) { ok = false; break; }
-        tc_fence_after_sync();
         for (int j = 0; j <= u.nkv && ok; ++j) {
-          int ks = 0, vs = 0;
-          if (j < u.nkv) {
-            ks = kuse % NK;
-            if (!wait_phase(bar(BAR_K_READY + ks), (kuse / NK) & 1, abort_flag, lim, 31)) { ok = false; break; }
-          }
-          if (j >= 1) {
-            vs = vuse % NV;
-            if (!wait_phase(bar(BAR_V_FULL + vs), (vuse / NV) & 1, abort_flag, lim, 32)) { ok = false; break; }
-          }
+          const int ks = kslot, vs = vslot;
+          if (j < u.nkv && !wait_phase(bar(BAR_K_READY + ks), kph, abort_flag, lim, 31)) { ok = false; break; }
+          if (j >= 1 && !wait_phase(bar(BAR_V_FULL + vs), vph, abort_flag, lim, 32)) { ok = false; break; }
+          const uint64_t dk = dk0 + ks * kstep, dks = dks0 + ks * kstep, dv = dv0 + vs * vstep;
           tc_fence_after_sync();
+#pragma unroll
           for (int tau = 0; tau < 2; ++tau) {
             const int n = tau == 0 ? u.n0 : u.n1;
             if (n == 0) continue;
@@ -263,35 +298,47 @@ __global__ void __launch_bounds__(kWsThreads, 1)
               if (!wait_phase(bar(BAR_P_FULL + tau), p_cnt[tau] & 1, abort_flag, lim, 33)) { ok = false; break; }
               ++p_cnt[tau];
               tc_fence_after_sync();
-              const uint32_t vlo = desc_lo_v(smem_u32(smem + L.v[vs]));
+              mma_ts(tO, tS, dv, idesc_pv, j > 1);
 #pragma unroll
-              for (int kk = 0; kk < kRows / 16; ++kk)
-                mma_ts(tO, tS + kk * 8, desc_of(vlo + kk * 64), idesc_pv, (j > 1 || kk > 0));
+              for (int kk = 1; kk < kRows / 16; ++kk) mma_ts(tO, tS + kk * 8, dv + kk * 64, idesc_pv, 1);
               issued = true;
               if (j == n) tc_commit(bar(BAR_O_FINAL + tau));
             }
             if (j < n) {
-              const uint32_t q = desc_lo_k(smem_u32(smem + L.q_raw[tau]));
-              const uint32_t qs = desc_lo_k(smem_u32(smem + L.q_side[tau]));
-              const uint32_t kr = desc_lo_k(smem_u32(smem + L.k_raw[ks]));
-              const uint32_t ksd = desc_lo_k(smem_u32(smem + L.k_side[ks]));
+              if (j == 0) {
+                const uint32_t par = tau == 0 ? (u_local & 1) : (q1_cnt++ & 1);
+                if (!wait_phase(bar(tau == 0 ? BAR_Q_READY : BAR_Q_READY1), par, abort_flag, lim, 30)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after_sync();
+              }
+              const uint64_t q = dq[tau], qs = dqs[tau];
+              mma_ss(tS, q, dk, idesc_s, 0);
 #pragma unroll
-              for (int kc = 0; kc < D / 16; ++kc)
-                mma_ss(tS, desc_of(q + kchunk_off(kc)), desc_of(kr + kchunk_off(kc)), idesc_s, kc > 0);
+              for (int kc = 1; kc < D / 16; ++kc) mma_ss(tS, q + kchunk_off(kc), dk + kchunk_off(kc), idesc_s, 1);
+              // a plain runtime loop: the same issue written as an unrolled loop of 8 with a
+              // `kc < nside` guard produced wrong scores for nside >= 2 on the GPU
               for (int kc = 0; kc < nside; ++kc) {
-                const uint32_t o = kchunk_off(kc);
-                mma_ss(tS, desc_of(qs + o), desc_of(kr + o), idesc_s, 1);
-                mma_ss(tS, desc_of(q + o), desc_of(ksd + o), idesc_s, 1);
+                mma_ss(tS, qs + kchunk_off(kc), dk + kchunk_off(kc), idesc_s, 1);
+                mma_ss(tS, q + kchunk_off(kc), dks + kchunk_off(kc), idesc_s, 1);
               }
               issued = true;
               tc_commit(bar(BAR_S_FULL + tau));
             }
           }
           if (!ok) break;
-          if (j < u.nkv) { tc_commit(bar(BAR_K_EMPTY + ks)); ++kuse; }
-          if (j >= 1) { tc_commit(bar(BAR_V_EMPTY + vs)); ++vuse; }
+          if (j < u.nkv) {
+            tc_commit(bar(BAR_K_EMPTY + ks));
+            if (++kslot == NK) { kslot = 0; kph ^= 1; }
+          }
+          if (j >= 1) {
+            tc_commit(bar(BAR_V_EMPTY + vs));
+            if (++vslot == NV) { vslot = 0; vph ^= 1; }
+          }
+          // the unit's last S MMAs are issued: its query buffers may be refilled
+          if (j == u.nkv - 1) tc_commit(bar(BAR_Q_EMPTY));
         }
-        tc_commit(bar(BAR_Q_EMPTY));
         ++u_local;
       }
       if (issued && (!ok || *abort_flag)) {
@@ -301,69 +348,76 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     }
    } else {
     // ======================================================= rotary transform ====
-    const int tt = tid - 64;  // 0..63: rows tt and tt + 64
+    // Per unit the tiles arrive as: query tile 0, query tile 1 (if any), K_0, K_1, ...
+    // One loop over that list, one rotation call site.
+    const int tt = tid - 64;  // 0..63: rows tt and tt + 64 of every tile
     const int h = p.r >> 1;
-    // 0: no rotary.  With the table of the next tile loaded one K block ahead:
-    // 1: r = 8, 3: r = 24 (whole rotated prefix in registers), 2: r = 16, 4: r = 32
-    // (groups of 8 pairs).  5: r % 16 == 0 and r > 32, groups with their table loads
-    // double-buffered inside the tile.  6: anything else, the scalar path.
-    int kind = 0;
-    if (p.r > 0) kind = (p.r % 8 == 0 && p.r <= 32) ? p.r / 8 : ((p.r % 16 == 0) ? 5 : 6);
-    auto kpos = [&](int j, int row) -> int64_t {
-      const int64_t pos = static_cast<int64_t>(j) * kRows + row;
+    constexpr int AH = rot_ahead(RK);
+    float4 ta0[8], ta1[8];  // table entries of rows tt / tt + 64, loaded one tile ahead
+    auto pos_of = [&](int blk, int row) -> int64_t {
+      const int64_t pos = static_cast<int64_t>(blk) * kRows + row;
       return pos < p.S ? pos : -1;
     };
-    float4 tn0[8], tn1[8];  // table entries of rows tt, tt + 64 of the next tile (kinds 1..4)
-    auto prefetch = [&](int64_t p0, int64_t p1) {
-      switch (kind) {
-        case 1: cs_load_n<2>(tn0, p.cs, h, 0, p0); cs_load_n<2>(tn1, p.cs, h, 0, p1); break;
-        case 2: cs_load_n<4>(tn0, p.cs, h, 0, p0); cs_load_n<4>(tn1, p.cs, h, 0, p1); break;
-        case 3: cs_load_n<6>(tn0, p.cs, h, 0, p0); cs_load_n<6>(tn1, p.cs, h, 0, p1); break;
-        case 4: cs_load_n<8>(tn0, p.cs, h, 0, p0); cs_load_n<8>(tn1, p.cs, h, 0, p1); break;
-        default: break;
+    auto load_ahead = [&](int blk) {
+      if (AH > 0) {
+        cs_load_n<AH>(ta0, p.cs, h, 0, pos_of(blk, tt));
+        cs_load_n<AH>(ta1, p.cs, h, 0, pos_of(blk, tt + 64));
       }
     };
-    auto rotate = [&](uint8_t* tile, uint8_t* side, int64_t p0, int64_t p1) {
-      switch (kind) {
-        case 1: rotate_row_small<1>(tile, side, tt, tn0); rotate_row_small<1>(tile, side, tt + 64, tn1); break;
-        case 3: rotate_row_small<3>(tile, side, tt, tn0); rotate_row_small<3>(tile, side, tt + 64, tn1); break;
-        case 4:
-          rotate_group8(tile, side, tt, 8, h, tn0 + 4);
-          rotate_group8(tile, side, tt + 64, 8, h, tn1 + 4);  // fallthrough to group 0
-        case 2:
-          rotate_group8(tile, side, tt, 0, h, tn0);
-          rotate_group8(tile, side, tt + 64, 0, h, tn1);
-          break;
-        case 5: rotate_two_rows_groups(tile, side, tt, tt + 64, p0, p1, p.cs, h, tn0, tn1); break;
-        case 6: rotate_row(tile, side, tt, p0, p.cs, p.r); rotate_row(tile, side, tt + 64, p1, p.cs, p.r); break;
-        default: break;
-      }
-    };
-    uint32_t kuse = 0, u_local = 0;
-    for (int rd = 0; rd * G < p.num_units; ++rd) {
+    int kslot = 0;
+    uint32_t kph = 0, u_local = 0;
+    bool ok = true;
+    int rd0 = 0;
+    while (rd0 * G < p.num_units && snake_unit(rd0, blockIdx.x, G) >= p.num_units) ++rd0;
+    if (AH > 0 && rd0 * G < p.num_units) load_ahead(2 * decode_unit(snake_unit(rd0, blockIdx.x, G), p.B, p.H, p.S).t);
+    for (int rd = rd0; rd * G < p.num_units && ok; ++rd) {
       const int k = snake_unit(rd, blockIdx.x, G);
       if (k >= p.num_units) continue;
       const Unit u = decode_unit(k, p.B, p.H, p.S);
-      if (!wait_phase(bar(BAR_Q_FULL), u_local & 1, abort_flag, lim, 20)) break;
-      for (int t = 0; t < (u.n1 > 0 ? 2 : 1) && kind > 0; ++t) {
-        const int qt = 2 * u.t + t;
-        prefetch(kpos(qt, tt), kpos(qt, tt + 64));
-        rotate(smem + L.q_raw[t], smem + L.q_side[t], kpos(qt, tt), kpos(qt, tt + 64));
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(BAR_Q_READY));
-      prefetch(kpos(0, tt), kpos(0, tt + 64));
-      bool ok = true;
-      for (int j = 0; j < u.nkv; ++j) {
-        const int s = kuse % NK;
-        if (!wait_phase(bar(BAR_K_FULL + s), (kuse / NK) & 1, abort_flag, lim, 21)) { ok = false; break; }
-        rotate(smem + L.k_raw[s], smem + L.k_side[s], kpos(j, tt), kpos(j, tt + 64));
+      const int nq = u.n1 > 0 ? 2 : 1;
+#pragma unroll 1
+      for (int it = 0; it < nq + u.nkv; ++it) {
+        const bool isq = it < nq;
+        const int s = kslot;
+        const int blk = isq ? 2 * u.t + it : it - nq;  // 128-row block of the sequence
+        if (isq ? (it == 0 && !wait_phase(bar(BAR_Q_FULL), u_local & 1, abort_flag, lim, 20))
+                : !wait_phase(bar(BAR_K_FULL + s), kph, abort_flag, lim, 21)) {
+          ok = false;
+          break;
+        }
+        uint8_t* tile = smem + (isq ? L.q_raw[it] : L.k_raw[s]);
+        uint8_t* side = smem + (isq ? L.q_side[it] : L.k_side[s]);
+        if (RK == kRotR24) {
+          rotate_row_small<3>(tile, side, tt, ta0);
+          rotate_row_small<3>(tile, side, tt + 64, ta1);
+        } else if (RK == kRotR16 || RK == kRotR32) {
+#pragma unroll
+          for (int g = 0; g < AH / 4; ++g) {
+            rotate_group8(tile, side, tt, 8 * g, h, ta0 + 4 * g);
+            rotate_group8(tile, side, tt + 64, 8 * g, h, ta1 + 4 * g);
+          }
+        } else if (RK == kRotGroups) {
+          rotate_two_rows_groups(tile, side, tt, tt + 64, pos_of(blk, tt), pos_of(blk, tt + 64), p.cs, h, ta0, ta1);
+        } else if (RK == kRotScalar) {
+          rotate_row(tile, side, tt, pos_of(blk, tt), p.cs, p.r);
+          rotate_row(tile, side, tt + 64, pos_of(blk, tt + 64), p.cs, p.r);
+        }
         fence_proxy_async_smem();
-        mbar_arrive(bar(BAR_K_READY + s));
-        ++kuse;
-        if (j + 1 < u.nkv) prefetch(kpos(j + 1, tt), kpos(j + 1, tt + 64));
+        mbar_arrive(bar(isq ? (it == 0 ? BAR_Q_READY : BAR_Q_READY1) : BAR_K_READY + s));
+        if (!isq && ++kslot == NK) {
+          kslot = 0;
+          kph ^= 1;
+        }
+        // table entries of the next tile in this list, or of the next unit's query tile 0
+        if (AH > 0) {
+          if (it + 1 < nq + u.nkv) {
+            load_ahead(it + 1 < nq ? 2 * u.t + it + 1 : it + 1 - nq);
+          } else {
+            const int kn = snake_unit(rd + 1, blockIdx.x, G);
+            if (kn < p.num_units) load_ahead(2 * decode_unit(kn, p.B, p.H, p.S).t);
+          }
+        }
       }
-      if (!ok) break;
       ++u_local;
     }
    }
@@ -385,14 +439,17 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const int qt = 2 * u.t + tau;
       float m_used = -INFINITY, l_run = 0.0f;
       bool ok = true;
+#pragma unroll 1
       for (int j = 0; j < n; ++j) {
-        if (!wait_phase(bar(BAR_S_FULL + tau), s_use & 1, abort_flag, lim, 40)) { ok = false; break; }
+        if (!wait_phase_inline(bar(BAR_S_FULL + tau), s_use & 1, abort_flag, lim, 40)) { ok = false; break; }
         ++s_use;
         tc_fence_after_sync();
         uint32_t sr[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
         tmem_wait_ld();
+        // causal mask on the diagonal block: keys > row get -inf (the block's keys are
+        // 128*qt + c, its rows 128*qt + row)
         if (j == qt) {
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -458,7 +515,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         mbar_arrive(bar(BAR_P_FULL + tau));
       }
       if (!ok) break;
-      if (!wait_phase(bar(BAR_O_FINAL + tau), o_use & 1, abort_flag, lim, 41)) break;
+      if (!wait_phase_inline(bar(BAR_O_FINAL + tau), o_use & 1, abort_flag, lim, 41)) break;
       ++o_use;
       tc_fence_after_sync();
       const int qrow = qt * kRows + row;
@@ -494,17 +551,28 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   }
 }
 
-// Ring depths per head dim (shared memory <= 227 KB with the side tiles of r <= 64).
-template <int D>
-struct WsConfig;
-template <> struct WsConfig<64> { static constexpr int NK = 4, NV = 4; };
-template <> struct WsConfig<96> { static constexpr int NK = 3, NV = 2; };
-template <> struct WsConfig<128> { static constexpr int NK = 2, NV = 2; };
+constexpr int kSmemLimit = 227 * 1024;
 
-template <int D, int NK, int NV>
+// Ring depths: the deepest (K, V) pair that fits next to the two query tiles, preferring
+// the per-head-dim defaults.
+inline void pick_rings(int D, int side_cols, int* nk, int* nv) {
+  const int pref_k = D == 64 ? 4 : D == 96 ? 3 : 2, pref_v = D == 64 ? 4 : 2;
+  const int cand[][2] = {{pref_k, pref_v}, {3, 2}, {2, 2}, {2, 1}, {1, 1}};
+  for (const auto& c : cand) {
+    if (ws_layout(D, side_cols, c[0], c[1]).total <= kSmemLimit) {
+      *nk = c[0];
+      *nv = c[1];
+      return;
+    }
+  }
+  *nk = *nv = 1;
+}
+
+template <int D, int RK>
 int launch_ws_impl(const CUtensorMap& map, AttnParams p, int num_sms, cudaStream_t stream, int* last_err) {
-  const WsLayout L = ws_layout(D, p.side_cols, NK, NV);
-  auto kern = attn_fwd_ws_kernel<D, NK, NV>;
+  pick_rings(D, p.side_cols, &p.nk, &p.nv);
+  const WsLayout L = ws_layout(D, p.side_cols, p.nk, p.nv);
+  auto kern = attn_fwd_ws_kernel<D, RK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   const int T = (p.S + 255) / 256;
@@ -516,16 +584,16 @@ int launch_ws_impl(const CUtensorMap& map, AttnParams p, int num_sms, cudaStream
   return 0;
 }
 
-constexpr int kSmemLimit = 227 * 1024;
-
-// Picks ring depths that fit: the configured ones, else shallower rings for wide side tiles.
 template <int D>
 int launch_attn_ws(const CUtensorMap& map, const AttnParams& p, int num_sms, cudaStream_t stream, int* last_err) {
-  constexpr int NK = WsConfig<D>::NK, NV = WsConfig<D>::NV;
-  if (ws_layout(D, p.side_cols, NK, NV).total <= kSmemLimit) return launch_ws_impl<D, NK, NV>(map, p, num_sms, stream, last_err);
-  if (ws_layout(D, p.side_cols, 2, 2).total <= kSmemLimit) return launch_ws_impl<D, 2, 2>(map, p, num_sms, stream, last_err);
-  if (ws_layout(D, p.side_cols, 2, 1).total <= kSmemLimit) return launch_ws_impl<D, 2, 1>(map, p, num_sms, stream, last_err);
-  return launch_ws_impl<D, 1, 1>(map, p, num_sms, stream, last_err);
+  switch (rot_kind(p.r)) {
+    case kRotNone: return launch_ws_impl<D, kRotNone>(map, p, num_sms, stream, last_err);
+    case kRotR16: return launch_ws_impl<D, kRotR16>(map, p, num_sms, stream, last_err);
+    case kRotR24: return launch_ws_impl<D, kRotR24>(map, p, num_sms, stream, last_err);
+    case kRotR32: return launch_ws_impl<D, kRotR32>(map, p, num_sms, stream, last_err);
+    case kRotGroups: return launch_ws_impl<D, kRotGroups>(map, p, num_sms, stream, last_err);
+    default: return launch_ws_impl<D, kRotScalar>(map, p, num_sms, stream, last_err);
+  }
 }
 
 }  // namespace neox

@@ -81,6 +81,17 @@ def test_large_workloads_sampled_rows(name):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
 
 
+@pytest.mark.parametrize("B,S,H,D,r", [
+    (4, 300, 40, 64, 16),    # 320 units: CTAs run several, half of them without a second query tile
+    (3, 1100, 50, 96, 24),   # 750 units, ragged last block with a second tile of 76 rows
+    (2, 650, 48, 128, 32),   # 288 units, last block without a second tile
+])
+def test_many_units_per_cta_ragged(B, S, H, D, r):
+    # more units than SMs, so each persistent CTA walks several units, mixing units with
+    # and without a second query tile; every row is checked
+    full_check(B, S, H, D, r, seed=B * S + H)
+
+
 def test_deterministic_and_causal_on_gpu():
     B, S, H, D, r = 1, 600, 2, 96, 24
     qkv = make_qkv(B, S, H, D, seed=5)
