@@ -266,6 +266,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // descriptor is a base below plus a constant: the issue loop is adds and MMAs only.
       const uint64_t dq[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_raw[0]))),
                               desc_of(desc_lo_k(smem_u32(smem + L.q_raw[1])))};
+      // query descriptors of every 16-column chunk, both tiles (fixed for the kernel)
+      uint64_t qd[2][D / 16];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int kc = 0; kc < D / 16; ++kc) qd[t][kc] = dq[t] + kchunk_off(kc);
       const uint64_t dqs[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_side[0]))),
                                desc_of(desc_lo_k(smem_u32(smem + L.q_side[1])))};
       const uint64_t dk0 = desc_of(desc_lo_k(smem_u32(smem + L.k_raw[0])));
@@ -287,7 +293,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           const int ks = kslot, vs = vslot;
           if (j < u.nkv && !wait_phase(bar(BAR_K_READY + ks), kph, abort_flag, lim, 31)) { ok = false; break; }
           if (j >= 1 && !wait_phase(bar(BAR_V_FULL + vs), vph, abort_flag, lim, 32)) { ok = false; break; }
+          // this step's K and V descriptors, computed once for both tiles
           const uint64_t dk = dk0 + ks * kstep, dks = dks0 + ks * kstep, dv = dv0 + vs * vstep;
+          uint64_t kd[D / 16], vd[kRows / 16];
+#pragma unroll
+          for (int kc = 0; kc < D / 16; ++kc) kd[kc] = dk + kchunk_off(kc);
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk) vd[kk] = dv + kk * 64;
           tc_fence_after_sync();
 #pragma unroll
           for (int tau = 0; tau < 2; ++tau) {
@@ -298,9 +310,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
               if (!wait_phase(bar(BAR_P_FULL + tau), p_cnt[tau] & 1, abort_flag, lim, 33)) { ok = false; break; }
               ++p_cnt[tau];
               tc_fence_after_sync();
-              mma_ts(tO, tS, dv, idesc_pv, j > 1);
-#pragma unroll
-              for (int kk = 1; kk < kRows / 16; ++kk) mma_ts(tO, tS + kk * 8, dv + kk * 64, idesc_pv, 1);
+              mma_ts_x8(tO, tS, vd, idesc_pv, j > 1);
               issued = true;
               if (j == n) tc_commit(bar(BAR_O_FINAL + tau));
             }
@@ -314,14 +324,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after_sync();
               }
               const uint64_t q = dq[tau], qs = dqs[tau];
-              mma_ss(tS, q, dk, idesc_s, 0);
+              mma_ss(tS, qd[tau][0], kd[0], idesc_s, 0);
 #pragma unroll
-              for (int kc = 1; kc < D / 16; ++kc) mma_ss(tS, q + kchunk_off(kc), dk + kchunk_off(kc), idesc_s, 1);
+              for (int kc = 1; kc < D / 16; ++kc) mma_ss_acc(tS, qd[tau][kc], kd[kc], idesc_s);
               // a plain runtime loop: the same issue written as an unrolled loop of 8 with a
               // `kc < nside` guard produced wrong scores for nside >= 2 on the GPU
               for (int kc = 0; kc < nside; ++kc) {
-                mma_ss(tS, qs + kchunk_off(kc), dk + kchunk_off(kc), idesc_s, 1);
-                mma_ss(tS, q + kchunk_off(kc), dks + kchunk_off(kc), idesc_s, 1);
+                mma_ss_acc(tS, qs + kchunk_off(kc), dk + kchunk_off(kc), idesc_s);
+                mma_ss_acc(tS, q + kchunk_off(kc), dks + kchunk_off(kc), idesc_s);
               }
               issued = true;
               tc_commit(bar(BAR_S_FULL + tau));

@@ -132,6 +132,34 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Eight back-to-back MMAs D (+)= A(tmem cols a, a+8, ..., a+56) * B(b[i]), i = 0..7, the
+// first accumulating only if acc != 0: one asm block, one predicate, no address math.
+__device__ __forceinline__ void mma_ts_x8(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[8], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, p;\n\t"
+      "add.u32 a, %1, 8;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %3, %11, t;\n\t"
+      "add.u32 a, %1, 16;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %4, %11, t;\n\t"
+      "add.u32 a, %1, 24;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %5, %11, t;\n\t"
+      "add.u32 a, %1, 32;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %6, %11, t;\n\t"
+      "add.u32 a, %1, 40;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %7, %11, t;\n\t"
+      "add.u32 a, %1, 48;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %8, %11, t;\n\t"
+      "add.u32 a, %1, 56;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [a], %9, %11, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc),
+      "r"(idesc)
+      : "memory");
+}
+// D(tmem) += A(smem desc) * B(smem desc), always accumulating (constant predicate).
+__device__ __forceinline__ void mma_ss_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred t;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
