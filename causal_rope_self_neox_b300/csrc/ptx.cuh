@@ -160,6 +160,59 @@ __device__ __forceinline__ void mma_ss_acc(uint32_t d_tmem, uint64_t adesc, uint
       : "memory");
 }
 
+// ---- the same tensor-core operations issued from a converged warp ----
+// The whole warp runs the issue loop (uniform control flow, so loop state and descriptors
+// stay warp-uniform); `lead` is 1 in exactly one lane, the one that starts each operation.
+__device__ __forceinline__ uint32_t elect_lane() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void tc_commit_l(uint32_t lead, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+      "r"(lead)
+      : "memory");
+}
+// D (+)= A(smem) * B(smem); accumulates only if acc != 0.
+__device__ __forceinline__ void mma_ss_l(uint32_t lead, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 e, %5, 0;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(lead)
+      : "memory");
+}
+// D += A(smem) * B(smem).
+__device__ __forceinline__ void mma_ss_acc_l(uint32_t lead, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred t, e;\n\tsetp.ne.b32 e, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, t;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(lead)
+      : "memory");
+}
+// Eight MMAs D (+)= A(tmem cols a, a+8, ..., a+56) * B(b[i]), the first accumulating only if
+// acc != 0.
+__device__ __forceinline__ void mma_ts_x8_l(uint32_t lead, uint32_t d_tmem, uint32_t a_tmem,
+                                            const uint64_t (&b)[8], uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, t, e;\n\t.reg .b32 a;\n\t"
+      "setp.ne.b32 e, %12, 0;\n\tsetp.ne.b32 p, %10, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, p;\n\t"
+      "add.u32 a, %1, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %3, %11, t;\n\t"
+      "add.u32 a, %1, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %4, %11, t;\n\t"
+      "add.u32 a, %1, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %5, %11, t;\n\t"
+      "add.u32 a, %1, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %6, %11, t;\n\t"
+      "add.u32 a, %1, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %7, %11, t;\n\t"
+      "add.u32 a, %1, 48;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %8, %11, t;\n\t"
+      "add.u32 a, %1, 56;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], %9, %11, t;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc),
+      "r"(idesc), "r"(lead)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
