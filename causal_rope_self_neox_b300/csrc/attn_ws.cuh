@@ -260,10 +260,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
    } else if (warp == 1) {
     // ============================================================ MMA issuer ====
     // The whole warp walks the schedule, so its control flow and descriptors stay
-    // warp-uniform; one elected lane starts each tensor-core operation.  The only waits
-    // here are P_tau (per tile and block) and, once per unit, K_0 and the query tiles:
-    // readiness of V_j and K_{j+1} is checked by the softmax warps before they publish
-    // P_tau(j), and the ring slots are released by the softmax warps as well.
+    // warp-uniform (a single-lane issue loop runs markedly slower once the softmax warps
+    // on the same SM sub-partition are busy); one elected lane starts each tensor-core
+    // operation.  Ring slots and query buffers are released by commits, i.e. as soon as
+    // the MMAs reading them have completed.
     {
       const uint32_t lead = elect_lane();
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const uint32_t kstep = static_cast<uint32_t>(tile_bytes(D) + tile_bytes(p.side_cols)) >> 4;
       const uint32_t vstep = static_cast<uint32_t>(tile_bytes(D)) >> 4;
       int kslot = 0, vslot = 0;
-      uint32_t kph = 0, u_local = 0;
+      uint32_t kph = 0, vph = 0, u_local = 0;
       uint32_t p_cnt[2] = {0, 0};
       uint32_t q1_cnt = 0;  // units with a query tile 1 (a ragged last block may have none)
       const int nside = p.r16 / 16;  // 16-column chunks of lo products (<= 8)
@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const Unit u = decode_unit(k, p.B, p.H, p.S);
         for (int j = 0; j <= u.nkv && ok; ++j) {
           const int ks = kslot, vs = vslot;
-          // block 0 of a unit: nothing before it has checked K_0
-          if (j == 0 && !wait_all(BAR_K_READY + ks, kph, 31)) { ok = false; break; }
+          if (j < u.nkv && !wait_all(BAR_K_READY + ks, kph, 31)) { ok = false; break; }
+          if (j >= 1 && !wait_all(BAR_V_FULL + vs, vph, 32)) { ok = false; break; }
           // this step's K and V descriptors, computed once for both tiles
           const uint64_t dk = dk0 + ks * kstep, dks = dks0 + ks * kstep, dv = dv0 + vs * vstep;
           uint64_t kd[D / 16], vd[kRows / 16];
@@ -315,7 +315,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (n == 0) continue;
             const uint32_t tS = tmem + tau * 128, tO = tmem + 256 + tau * 128;
             if (j >= 1 && j <= n) {
-              // P_tau(j-1) published: V_{j-1} and (if j < n) K_j are ready as well
               if (!wait_all(BAR_P_FULL + tau, p_cnt[tau] & 1, 33)) { ok = false; break; }
               ++p_cnt[tau];
               tc_fence_after_sync();
@@ -344,8 +343,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             }
           }
           if (!ok) break;
-          if (j < u.nkv && ++kslot == NK) { kslot = 0; kph ^= 1; }
-          if (j >= 1 && ++vslot == NV) vslot = 0;
+          if (j < u.nkv) {
+            tc_commit_l(lead, bar(BAR_K_EMPTY + ks));
+            if (++kslot == NK) { kslot = 0; kph ^= 1; }
+          }
+          if (j >= 1) {
+            tc_commit_l(lead, bar(BAR_V_EMPTY + vs));
+            if (++vslot == NV) { vslot = 0; vph ^= 1; }
+          }
+          // the unit's last S MMAs are issued: its query buffers may be refilled
+          if (j == u.nkv - 1) tc_commit_l(lead, bar(BAR_Q_EMPTY));
         }
         ++u_local;
       }
@@ -439,44 +446,25 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t tS = tmem + tau * 128 + lane_off, tO = tmem + 256 + tau * 128 + lane_off;
     const float sl2 = p.scale_log2;
     uint32_t s_use = 0, o_use = 0;
-    // Ring bookkeeping, kept by the first thread of the warpgroup: the slot and lap parity
-    // of K_j and V_j for the block j being processed, and the slot of V_{j-1}.
-    const bool keeper = row == 0;
-    int ksl = 0, vsl = 0, vprev = 0;
-    uint32_t kpar = 0, vpar = 0;
-    auto advance = [&]() {
-      if (++ksl == NK) { ksl = 0; kpar ^= 1; }
-      vprev = vsl;
-      if (++vsl == NV) { vsl = 0; vpar ^= 1; }
-    };
     for (int rd = 0; rd * G < p.num_units; ++rd) {
       const int k = snake_unit(rd, blockIdx.x, G);
       if (k >= p.num_units) continue;
       const Unit u = decode_unit(k, p.B, p.H, p.S);
       const int n = tau == 0 ? u.n0 : u.n1;
-      if (n == 0) {  // no query tile 1 in this unit: only follow the rings
-        if (keeper)
-          for (int i = 0; i < u.nkv; ++i) advance();
-        continue;
-      }
-      // The tile that reads every block of the unit last (tile 1 if the unit has one)
-      // releases the ring slots and the query buffers: the MMAs are issued in order
-      // PV_0, S_0, PV_1, S_1 per block, and a commit tracks every earlier MMA, so its
-      // S(j) landing means both tiles are done with K_j and V_{j-1}.
-      const bool releaser = keeper && tau == (u.n1 > 0 ? 1 : 0);
+      if (n == 0) continue;
       const int qt = 2 * u.t + tau;
       float m_used = -INFINITY, l_run = 0.0f;
+      // every exit decision is warp-uniform: the TMEM loads and stores below are
+      // warp-collective, so no lane may leave while the others go on
       bool ok = true;
 #pragma unroll 1
       for (int j = 0; j < n; ++j) {
-        if (!wait_phase_inline(bar(BAR_S_FULL + tau), s_use & 1, abort_flag, lim, 40)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_phase_inline(bar(BAR_S_FULL + tau), s_use & 1, abort_flag, lim, 40))) {
+          ok = false;
+          break;
+        }
         ++s_use;
         tc_fence_after_sync();
-        if (releaser) {
-          mbar_arrive(bar(BAR_K_EMPTY + ksl));
-          if (j >= 1) mbar_arrive(bar(BAR_V_EMPTY + vprev));
-          if (j == n - 1) mbar_arrive(bar(BAR_Q_EMPTY));
-        }
         uint32_t sr[128];
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
@@ -545,27 +533,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         tmem_st32(tS + 32, pk + 32);
         tmem_wait_st();
         tc_fence_before_sync();
-        if (keeper) {
-          // the MMAs that follow P(j) read V_j (PV) and, if this tile has another block,
-          // K_{j+1} (next S): publish P only once both are in shared memory
-          const int kn = ksl + 1 == NK ? 0 : ksl + 1;
-          const uint32_t kpn = kn == 0 ? kpar ^ 1 : kpar;
-          if (!wait_phase_inline(bar(BAR_V_FULL + vsl), vpar, abort_flag, lim, 42) ||
-              (j + 1 < n && !wait_phase_inline(bar(BAR_K_READY + kn), kpn, abort_flag, lim, 43))) {
-            ok = false;
-            break;
-          }
-          advance();
-        }
         mbar_arrive(bar(BAR_P_FULL + tau));
       }
       if (!ok) break;
-      // both tiles' ring positions move to the next unit's block 0
-      if (keeper && n < u.nkv) advance();
-      if (!wait_phase_inline(bar(BAR_O_FINAL + tau), o_use & 1, abort_flag, lim, 41)) break;
+      if (!__all_sync(0xffffffffu, wait_phase_inline(bar(BAR_O_FINAL + tau), o_use & 1, abort_flag, lim, 41))) break;
       ++o_use;
       tc_fence_after_sync();
-      if (releaser) mbar_arrive(bar(BAR_V_EMPTY + vprev));
       const int qrow = qt * kRows + row;
       const float inv_l = 1.0f / l_run;
 #pragma unroll 1
