@@ -550,10 +550,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
         for (int q = 0; q < 16; ++q)
           pk[q] = pack_bf16x2(__uint_as_float(o[2 * q]) * inv_l, __uint_as_float(o[2 * q + 1]) * inv_l);
-        if (qrow < p.S) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + ((static_cast<int64_t>(u.b) * p.S + qrow) * p.H + u.h) * D + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        if (qrow < p.S) {  // 32-byte stores: a row is 2D bytes, 32-byte aligned
+          uint16_t* dst = p.out + ((static_cast<int64_t>(u.b) * p.S + qrow) * p.H + u.h) * D + c0;
+          st_global_v8(dst, pk);
+          st_global_v8(dst + 16, pk + 8);
         }
       }
       if (qrow < p.S)
