@@ -332,11 +332,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
               mma_ss_l(lead, tS, qd[tau][0], kd[0], idesc_s, 0);
 #pragma unroll
               for (int kc = 1; kc < D / 16; ++kc) mma_ss_acc_l(lead, tS, qd[tau][kc], kd[kc], idesc_s);
-              // a plain runtime loop: the same issue written as an unrolled loop of 8 with a
-              // `kc < nside` guard produced wrong scores for nside >= 2 on the GPU
-              for (int kc = 0; kc < nside; ++kc) {
-                mma_ss_acc_l(lead, tS, qs + kchunk_off(kc), dk + kchunk_off(kc), idesc_s);
-                mma_ss_acc_l(lead, tS, q + kchunk_off(kc), dks + kchunk_off(kc), idesc_s);
+              if constexpr (RK == kRotR24) {
+                // cross terms: dims 0..15 as q_lo.k_hi and q_hi.k_lo, dims 16..23 packed into
+                // one chunk of the two side tiles ([lo | hi] . [hi | lo])
+                mma_ss_acc_l(lead, tS, qs, dk, idesc_s);
+                mma_ss_acc_l(lead, tS, q, dks, idesc_s);
+                mma_ss_acc_l(lead, tS, qs + kchunk_off(1), dks + kchunk_off(1), idesc_s);
+              } else {
+                // a plain runtime loop: the same issue written as an unrolled loop of 8 with a
+                // `kc < nside` guard produced wrong scores for nside >= 2 on the GPU
+                for (int kc = 0; kc < nside; ++kc) {
+                  mma_ss_acc_l(lead, tS, qs + kchunk_off(kc), dk + kchunk_off(kc), idesc_s);
+                  mma_ss_acc_l(lead, tS, q + kchunk_off(kc), dks + kchunk_off(kc), idesc_s);
+                }
               }
               issued = true;
               tc_commit_l(lead, bar(BAR_S_FULL + tau));
@@ -403,9 +411,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         uint8_t* tile = smem + (isq ? L.q_raw[it] : L.k_raw[s]);
         uint8_t* side = smem + (isq ? L.q_side[it] : L.k_side[s]);
-        if (RK == kRotR24) {
-          rotate_row_small<3>(tile, side, tt, ta0);
-          rotate_row_small<3>(tile, side, tt + 64, ta1);
+        if (RK == kRotR24) {  // packed cross terms of dims 16..23 (see the MMA issue)
+          rotate_row_small<3>(tile, side, tt, ta0, isq ? 1 : 2);
+          rotate_row_small<3>(tile, side, tt + 64, ta1, isq ? 1 : 2);
         } else if (RK == kRotR16 || RK == kRotR32) {
 #pragma unroll
           for (int g = 0; g < AH / 4; ++g) {

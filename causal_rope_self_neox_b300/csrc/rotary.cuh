@@ -202,9 +202,14 @@ __device__ __forceinline__ void cs_load_n(float4* t, const float2* __restrict__ 
 
 // r = 8 * NCH <= 32: the whole rotated prefix of the row lives in registers; NCH chunk
 // loads, then NCH hi stores (in place) and NCH lo stores (side tile).
+//
+// Packed last chunk (NCH odd, i.e. r % 16 == 8; pack != 0): the side tile's last 16-column
+// chunk holds both halves of the cross terms of the final 8 dims, so that one MMA chunk
+// accumulates q_lo.k_hi + q_hi.k_lo there instead of two half-empty chunks.  For a query
+// row (pack = 1) it is [lo | hi], for a key row (pack = 2) [hi | lo].
 template <int NCH>
 __device__ __forceinline__ void rotate_row_small(uint8_t* __restrict__ tile, uint8_t* __restrict__ side, int row,
-                                                 const float4* t) {
+                                                 const float4* t, int pack = 0) {
   constexpr int R = 8 * NCH, HH = R / 2;
   float x[R], y[R];
 #pragma unroll
@@ -221,7 +226,12 @@ __device__ __forceinline__ void rotate_row_small(uint8_t* __restrict__ tile, uin
     uint4 hi, lo;
     split8(y + 8 * c, hi, lo);
     *reinterpret_cast<uint4*>(tile + sw64_off(row, 8 * c)) = hi;
-    *reinterpret_cast<uint4*>(side + sw64_off(row, 8 * c)) = lo;
+    if ((NCH & 1) && c == NCH - 1 && pack != 0) {
+      *reinterpret_cast<uint4*>(side + sw64_off(row, 8 * c)) = pack == 1 ? lo : hi;
+      *reinterpret_cast<uint4*>(side + sw64_off(row, 8 * c + 8)) = pack == 1 ? hi : lo;
+    } else {
+      *reinterpret_cast<uint4*>(side + sw64_off(row, 8 * c)) = lo;
+    }
   }
 }
 
