@@ -97,3 +97,70 @@ def sample_rows(w: Workload, n: int = 256, extra_edges: bool = True) -> np.ndarr
         edges = sorted({e for e in (0, 1, 127, 128, w.S - 1) if 0 <= e < w.S})
         rows = np.concatenate([rows, np.array([[0, 0, e] for e in edges], dtype=np.int64)], axis=0)
     return rows
+
+
+# ------------------------------------------------------------------ decode ----
+# Incremental decode: one new token per sequence against a cache of earlier tokens.
+# The cache holds the projections as they came (keys not rotated), head-major
+# [B, H, Smax, D]; the new token's packed projection is [B, H, 3, D].
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    index: int
+    B: int
+    H: int
+    Smax: int
+    D: int
+    rotary_dim: int
+    pos: int  # tokens already cached in every sequence (the new token's position)
+    rotary_base: float = 10000.0
+
+    @property
+    def seed(self) -> int:
+        return 2000 + self.index
+
+    @property
+    def cache_bytes_read(self) -> int:
+        """K and V cache rows read per step (bf16): 2 * B * H * pos * D * 2."""
+        return 4 * self.B * self.H * self.pos * self.D
+
+    def describe(self) -> dict:
+        return {"workload": self.name, "B": self.B, "H": self.H, "Smax": self.Smax, "D": self.D,
+                "rotary_dim": self.rotary_dim, "rotary_base": self.rotary_base, "pos": self.pos,
+                "seed": self.seed}
+
+
+# serving-style batches at the end of a 2048-token context (GPT-NeoX family shapes)
+DECODE_WORKLOADS = {
+    "neox20b-decode": DecodeWorkload("neox20b-decode", 1, B=16, H=64, Smax=2048, D=96, rotary_dim=24, pos=2047),
+    "pythia1.4b-decode": DecodeWorkload("pythia1.4b-decode", 2, B=32, H=16, Smax=2048, D=128, rotary_dim=32,
+                                        pos=2047),
+    "pythia160m-decode": DecodeWorkload("pythia160m-decode", 3, B=64, H=12, Smax=2048, D=64, rotary_dim=16,
+                                        pos=2047),
+}
+
+
+def make_decode_inputs(B: int, H: int, Smax: int, D: int, seed: int):
+    """(qkv_new [B,H,3,D], k_cache [B,H,Smax,D], v_cache [B,H,Smax,D]) bf16 on the CPU, N(0,1)."""
+    g = torch.Generator().manual_seed(int(seed))
+    qkv_new = torch.randn((B, H, 3, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k_cache = torch.randn((B, H, Smax, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v_cache = torch.randn((B, H, Smax, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return qkv_new, k_cache, v_cache
+
+
+def decode_from_sequence(qkv: torch.Tensor, pos, Smax: int):
+    """Split a prefill input qkv[B,S,H,3,D] into decode inputs: for sequence b the cache gets
+    tokens 0..pos[b]-1 (rows >= pos[b] filled with a sentinel pattern that must never be read)
+    and the new token is token pos[b].  Pure data movement."""
+    B, S, H, _, D = qkv.shape
+    new = torch.empty((B, H, 3, D), dtype=qkv.dtype)
+    kc = torch.full((B, H, Smax, D), 12345.0, dtype=qkv.dtype)
+    vc = torch.full((B, H, Smax, D), -12345.0, dtype=qkv.dtype)
+    for b in range(B):
+        p = int(pos[b])
+        new[b] = qkv[b, p]
+        kc[b, :, :p] = qkv[b, :p, :, 1].permute(1, 0, 2)
+        vc[b, :, :p] = qkv[b, :p, :, 2].permute(1, 0, 2)
+    return new, kc, vc

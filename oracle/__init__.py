@@ -53,6 +53,8 @@ def _load():
             lib.neox_oracle_fwd_rows.restype = i32
             lib.neox_oracle_probs.argtypes = [P, i32, i32, i32, i32, i32, f64, i32, i32, i32, P]
             lib.neox_oracle_probs.restype = i32
+            lib.neox_oracle_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, i32]
+            lib.neox_oracle_decode.restype = i32
             _lib = lib
     return _lib
 
@@ -126,3 +128,29 @@ def probs(qkv_bits: np.ndarray, B: int, S: int, H: int, D: int, rotary_dim: int,
     if rc != 0:
         raise RuntimeError(f"neox_oracle_probs failed: {rc}")
     return p
+
+
+def decode(qkv_new_bits: np.ndarray, k_cache_bits, v_cache_bits, pos, B: int, H: int, Smax: int, D: int,
+           rotary_dim: int, base: float = 10000.0, threads: int | None = None):
+    """Incremental decode: one new token per sequence against a cache of earlier ones.
+
+    qkv_new_bits: bf16 bits [B,H,3,D] (the new token's packed projections);
+    k_cache_bits / v_cache_bits: bf16 bits [B,H,Smax,D], keys NOT rotated (rows p < pos[b]
+    are read, the rest ignored; may be None when every pos is 0);
+    pos: int [B], the new token's position (= tokens already cached), 0 <= pos < Smax.
+    Returns (out fp64 [B,H,D], lse fp64 [B,H]): by definition row pos[b] of the prefill.
+    """
+    q = _u16(qkv_new_bits, (B, H, 3, D))
+    kc = _u16(k_cache_bits, (B, H, Smax, D)) if k_cache_bits is not None else None
+    vc = _u16(v_cache_bits, (B, H, Smax, D)) if v_cache_bits is not None else None
+    p = np.ascontiguousarray(np.asarray(pos, dtype=np.int32))
+    if p.shape != (B,):
+        raise ValueError("pos must have shape [B]")
+    out = np.zeros((B, H, D), dtype=np.float64)
+    lse = np.zeros((B, H), dtype=np.float64)
+    rc = _load().neox_oracle_decode(_ptr(q), _ptr(kc) if kc is not None else None,
+                                    _ptr(vc) if vc is not None else None, _ptr(p), B, H, Smax, D, rotary_dim,
+                                    float(base), _ptr(out), _ptr(lse), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle decode failed ({rc})")
+    return out, lse

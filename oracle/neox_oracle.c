@@ -310,3 +310,114 @@ int neox_oracle_probs(const uint16_t* qkv, int B, int S, int H, int D, int r, do
   free(Kr); free(V); free(tmp); free(orow);
   return rc;
 }
+
+/* ------------------------------------------------------------------------------
+ * Incremental decode (one new token per sequence against a cache of earlier ones).
+ *
+ * The FasterTransformer guide ("GPT-NeoX on FasterTransformer", section "背景")
+ * names a per-token decoder that extends a growing context; it prints no
+ * interface.  Reading used here (listed in the design notes):
+ *  - sequence b already holds pos[b] tokens, at positions 0..pos[b]-1; the new
+ *    token sits at position pos[b];
+ *  - the cache keeps the projections as they came, keys NOT rotated:
+ *    k_cache[b,h,p,:], v_cache[b,h,p,:] for p < pos[b] (bf16, [B,H,Smax,D]);
+ *  - the new token's packed projection is qkv_new[b,h,0|1|2,:] (bf16, [B,H,3,D]),
+ *    the per-token [H,3,D] packing of the prefill input;
+ *  - the new query attends to keys 0..pos[b] (itself included), each rotated at
+ *    its own position exactly as in the prefill, scaled by 1/sqrt(D).
+ * The result is by definition row pos[b] of the prefill over the whole sequence.
+ * Cache rows p >= pos[b] are never read.
+ * out: fp64 [B,H,D];  lse: fp64 [B,H] (natural log).  Returns 0 or < 0.          */
+typedef struct {
+  const uint16_t *qkv_new, *k_cache, *v_cache;
+  const int* pos;
+  int B, H, Smax, D, r;
+  double base;
+  double *out, *lse;
+  pthread_mutex_t mu;
+  int64_t next, n_items;
+  int failed;
+} djob_t;
+
+static void* worker_decode(void* arg) {
+  djob_t* J = (djob_t*)arg;
+  const int D = J->D;
+  double* x = malloc(sizeof(double) * (size_t)D);
+  double* qr = malloc(sizeof(double) * (size_t)D);
+  double* kr = malloc(sizeof(double) * (size_t)D);
+  double* scores = malloc(sizeof(double) * (size_t)(J->Smax + 1));
+  if (!x || !qr || !kr || !scores) {
+    pthread_mutex_lock(&J->mu);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->mu);
+    free(x); free(qr); free(kr); free(scores);
+    return NULL;
+  }
+  const double scale = 1.0 / sqrt((double)D);
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    int64_t item = J->next < J->n_items ? J->next++ : -1;
+    pthread_mutex_unlock(&J->mu);
+    if (item < 0) break;
+    const int64_t b = item / J->H, h = item % J->H;
+    const int64_t P = J->pos[b];
+    const uint16_t* nq = J->qkv_new + ((b * J->H + h) * 3 + 0) * (int64_t)D;
+    for (int d = 0; d < D; ++d) x[d] = bf16_to_f64(nq[d]);
+    neox_oracle_rotate(x, D, J->r, J->base, P, qr);
+    /* scores of keys 0..P */
+    double m = -INFINITY;
+    for (int64_t p = 0; p <= P; ++p) {
+      const uint16_t* k = p < P ? J->k_cache + ((b * J->H + h) * J->Smax + p) * (int64_t)D
+                                : J->qkv_new + ((b * J->H + h) * 3 + 1) * (int64_t)D;
+      for (int d = 0; d < D; ++d) x[d] = bf16_to_f64(k[d]);
+      neox_oracle_rotate(x, D, J->r, J->base, p, kr);
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qr[d] * kr[d];
+      scores[p] = dot * scale;
+      if (scores[p] > m) m = scores[p];
+    }
+    double l = 0.0;
+    for (int64_t p = 0; p <= P; ++p) {
+      scores[p] = exp(scores[p] - m);
+      l += scores[p];
+    }
+    double* o = J->out + (b * J->H + h) * (int64_t)D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int64_t p = 0; p <= P; ++p) {
+      const uint16_t* v = p < P ? J->v_cache + ((b * J->H + h) * J->Smax + p) * (int64_t)D
+                                : J->qkv_new + ((b * J->H + h) * 3 + 2) * (int64_t)D;
+      const double w = scores[p] / l;
+      for (int d = 0; d < D; ++d) o[d] += w * bf16_to_f64(v[d]);
+    }
+    J->lse[b * J->H + h] = m + log(l);
+  }
+  free(x); free(qr); free(kr); free(scores);
+  return NULL;
+}
+
+int neox_oracle_decode(const uint16_t* qkv_new, const uint16_t* k_cache, const uint16_t* v_cache, const int* pos,
+                       int B, int H, int Smax, int D, int r, double base, double* out, double* lse, int threads) {
+  if (!qkv_new || !pos || !out || !lse || B < 1 || H < 1 || Smax < 1 || D < 1 || r < 0 || r > D || (r & 1) ||
+      !(base > 0.0))
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    if (pos[b] < 0 || pos[b] >= Smax) return ORACLE_ERR_ARG;
+    if (pos[b] > 0 && (!k_cache || !v_cache)) return ORACLE_ERR_ARG;
+  }
+  djob_t J;
+  memset(&J, 0, sizeof J);
+  J.qkv_new = qkv_new; J.k_cache = k_cache; J.v_cache = v_cache; J.pos = pos;
+  J.B = B; J.H = H; J.Smax = Smax; J.D = D; J.r = r; J.base = base; J.out = out; J.lse = lse;
+  J.n_items = (int64_t)B * H;
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pthread_t tid[256];
+  pthread_mutex_init(&J.mu, NULL);
+  int started = 0;
+  for (int t = 1; t < threads; ++t)
+    if (pthread_create(&tid[started], NULL, worker_decode, &J) == 0) ++started;
+  worker_decode(&J);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
