@@ -353,7 +353,7 @@ static void* worker_decode(void* arg) {
     free(x); free(qr); free(kr); free(scores);
     return NULL;
   }
-  const double scale = 1.0 / sqrt((double)D);
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
   for (;;) {
     pthread_mutex_lock(&J->mu);
     int64_t item = J->next < J->n_items ? J->next++ : -1;
@@ -373,7 +373,7 @@ static void* worker_decode(void* arg) {
       neox_oracle_rotate(x, D, J->r, J->base, p, kr);
       double dot = 0.0;
       for (int d = 0; d < D; ++d) dot += qr[d] * kr[d];
-      scores[p] = dot * scale;
+      scores[p] = dot * inv_sqrt_d;
       if (scores[p] > m) m = scores[p];
     }
     double l = 0.0;
