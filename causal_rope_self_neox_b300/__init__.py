@@ -23,10 +23,11 @@ NEOX_ERR_CUDA = -4
 NEOX_ERR_DEVICE_TIMEOUT = -5
 NEOX_ERR_NO_DEVICE_SUPPORT = -6
 NEOX_ERR_TOO_LARGE = -7
+NEOX_ERR_DEVICE_BAD_POSITION = -8
 
 EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
            "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
-           "neox_attn_version", "neox_attn_fwd_noalloc")
+           "neox_attn_version", "neox_attn_fwd_noalloc", "neox_attn_decode")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +52,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             for name in ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_fwd_noalloc"):
                 getattr(lib, name).argtypes = fwd_args
                 getattr(lib, name).restype = i32
+            lib.neox_attn_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
+            lib.neox_attn_decode.restype = i32
             lib.neox_attn_get_device_error.argtypes = []
             lib.neox_attn_get_device_error.restype = i32
             lib.neox_attn_status_string.argtypes = [i32]
@@ -88,6 +91,13 @@ def neox_attn_fwd_noalloc(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_d
     cudaMalloc.  Calls that overlap on the GPU share that table and race."""
     return load_library().neox_attn_fwd_noalloc(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr,
                                                 stream)
+
+
+def neox_attn_decode(qkv_new_ptr: int, k_cache_ptr: int, v_cache_ptr: int, pos_ptr: int, B: int, H: int, Smax: int,
+                     D: int, rotary_dim: int, rotary_base: float, out_ptr: int, lse_ptr: int, stream: int = 0) -> int:
+    """Raw call of the incremental decode (one new token per sequence against a K/V cache)."""
+    return load_library().neox_attn_decode(qkv_new_ptr, k_cache_ptr, v_cache_ptr, pos_ptr, B, H, Smax, D, rotary_dim,
+                                           rotary_base, out_ptr, lse_ptr, stream)
 
 
 def neox_attn_get_device_error() -> int:
@@ -150,6 +160,39 @@ def attn_fwd(qkv, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=N
                 stream.cuda_stream)
     if rc != NEOX_OK:
         raise NeoxAttnError(rc, "neox_attn_fwd")
+    return out, lse
+
+
+def attn_decode(qkv_new, k_cache, v_cache, pos, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=None,
+                stream=None):
+    """Incremental decode on CUDA tensors: ``qkv_new`` bf16 ``[B,H,3,D]``, caches bf16
+    ``[B,H,Smax,D]`` (keys not rotated; row ``pos[b]`` is overwritten with the new k/v),
+    ``pos`` int32 ``[B]`` on the device.  Returns ``(out[B,H,D] bf16, lse[B,H] fp32)``."""
+    import torch
+
+    if qkv_new.dim() != 4 or qkv_new.shape[2] != 3 or qkv_new.dtype != torch.bfloat16 or not qkv_new.is_cuda:
+        raise ValueError("qkv_new must be a CUDA bf16 tensor of shape [B, H, 3, D]")
+    B, H, _, D = qkv_new.shape
+    for c in (k_cache, v_cache):
+        if c.dim() != 4 or c.shape[0] != B or c.shape[1] != H or c.shape[3] != D or c.dtype != torch.bfloat16 \
+                or not c.is_cuda or not c.is_contiguous():
+            raise ValueError("caches must be contiguous CUDA bf16 tensors of shape [B, H, Smax, D]")
+    if pos.dtype != torch.int32 or pos.shape != (B,) or not pos.is_cuda:
+        raise ValueError("pos must be a CUDA int32 tensor of shape [B]")
+    if not qkv_new.is_contiguous():
+        raise ValueError("qkv_new must be contiguous")
+    Smax = k_cache.shape[2]
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.bfloat16, device=qkv_new.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=qkv_new.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv_new.device)
+    with torch.cuda.device(qkv_new.device):
+        rc = neox_attn_decode(qkv_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), pos.data_ptr(), B, H, Smax,
+                              D, rotary_dim, float(rotary_base), out.data_ptr(), lse.data_ptr(), stream.cuda_stream)
+    if rc != NEOX_OK:
+        raise NeoxAttnError(rc, "neox_attn_decode")
     return out, lse
 
 

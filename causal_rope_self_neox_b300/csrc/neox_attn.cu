@@ -15,6 +15,7 @@
 #include "attn_common.cuh"
 #include "attn_simple.cuh"
 #include "attn_ws.cuh"
+#include "decode.cuh"
 
 namespace {
 
@@ -204,6 +205,98 @@ int launch_ws(Prepared& P, cudaStream_t stream) {
   return rc == 0 ? NEOX_OK : NEOX_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------- decode ----
+// Per-device fp32 scratch for the partial results of the decode key-range splits.
+struct Scratch {
+  int device;
+  size_t bytes;
+  float* ptr;
+};
+std::vector<Scratch> g_scratch;  // guarded by g_tab_mu
+
+int get_scratch(int device, size_t bytes, float** out) {
+  std::lock_guard<std::mutex> lk(g_tab_mu);
+  for (auto it = g_scratch.begin(); it != g_scratch.end(); ++it) {
+    if (it->device == device) {
+      if (it->bytes >= bytes) {
+        *out = it->ptr;
+        return NEOX_OK;
+      }
+      cudaError_t e = cudaDeviceSynchronize();  // in-flight kernels may still use it
+      if (e != cudaSuccess) return cuda_fail(e);
+      cudaFree(it->ptr);
+      g_scratch.erase(it);
+      break;
+    }
+  }
+  const size_t grown = std::max<size_t>(bytes, size_t(1) << 20);
+  float* ptr = nullptr;
+  cudaError_t e = cudaMalloc(&ptr, grown);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_scratch.push_back(Scratch{device, grown, ptr});
+  *out = ptr;
+  return NEOX_OK;
+}
+
+// A K or V cache [B, H, Smax, D] as 128-row x 32-column boxes with the 64-byte swizzle
+// (the prefill's tile layout); rows past Smax read as zeros.
+int encode_cache_map(CUtensorMap* map, const void* cache, int B, int H, int Smax, int D) {
+  CUtensorMap dummy;
+  int rc = encode_qkv_map(&dummy, cache, 1, 1, 1, D);  // resolves the driver entry point once
+  if (rc != NEOX_OK) return rc;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Smax), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Smax) * D * 2,
+                           static_cast<cuuint64_t>(H) * Smax * D * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(neox::kBlkCols), static_cast<cuuint32_t>(neox::kRows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS ? NEOX_OK : cuda_fail(cudaErrorInvalidValue);
+}
+
+int validate_decode(const void* qkv_new, const void* k_cache, const void* v_cache, const int* pos, int B, int H,
+                    int Smax, int D, int r, float base, const void* out, const float* lse) {
+  if (!qkv_new || !k_cache || !v_cache || !pos || !out || !lse) return NEOX_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Smax < 1 || B > 65535 || H > 65535) return NEOX_ERR_INVALID_ARG;
+  if (D != 64 && D != 96 && D != 128) return NEOX_ERR_UNSUPPORTED_HEAD_DIM;
+  if (r < 0 || r > D || (r & 1)) return NEOX_ERR_INVALID_ARG;
+  if (!(base > 0.0f) || !std::isfinite(base)) return NEOX_ERR_INVALID_ARG;
+  const uint64_t cache_elems = static_cast<uint64_t>(B) * H * Smax * D;
+  if (cache_elems >= (1ull << 40)) return NEOX_ERR_INVALID_ARG;
+  for (const void* ptr : {qkv_new, k_cache, v_cache, out})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15) return NEOX_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3) || (reinterpret_cast<uintptr_t>(pos) & 3)) return NEOX_ERR_MISALIGNED;
+  const uint64_t bh = static_cast<uint64_t>(B) * H;
+  const struct {
+    const void* p;
+    uint64_t n;
+  } buf[6] = {{qkv_new, bh * 3 * D * 2}, {k_cache, cache_elems * 2}, {v_cache, cache_elems * 2},
+              {pos, static_cast<uint64_t>(B) * 4}, {out, bh * D * 2}, {lse, bh * 4}};
+  for (int i = 0; i < 6; ++i)
+    for (int j = i + 1; j < 6; ++j) {
+      if (i == 0 && j == 3) continue;  // the read-only inputs may share memory
+      if (ranges_overlap(reinterpret_cast<uintptr_t>(buf[i].p), buf[i].n, reinterpret_cast<uintptr_t>(buf[j].p),
+                         buf[j].n))
+        return NEOX_ERR_INVALID_ARG;
+    }
+  return NEOX_OK;
+}
+
+template <int D, bool SMALL_R>
+int launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const neox::DecodeParams& p, cudaStream_t stream) {
+  const int smem = neox::dec_smem_bytes(D);
+  cudaError_t e = cudaFuncSetAttribute(neox::attn_decode_kernel<D, SMALL_R>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  neox::attn_decode_kernel<D, SMALL_R><<<dim3(p.splits, p.H, p.B), neox::kDecThreads, smem, stream>>>(km, vm, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  neox::attn_decode_combine_kernel<D><<<dim3(p.H, p.B), 128, 0, stream>>>(p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
+}
+
 __global__ void selftest_wait_kernel(uint64_t limit_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -279,6 +372,61 @@ int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary
   }
 }
 
+int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const int* pos, int B, int H, int Smax,
+                     int D, int rotary_dim, float rotary_base, void* out, float* lse, void* stream_) {
+  try {
+    int rc = validate_decode(qkv_new, k_cache, v_cache, pos, B, H, Smax, D, rotary_dim, rotary_base, out, lse);
+    if (rc != NEOX_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int device = 0;
+    DeviceInfo dev;
+    rc = current_device(&device, &dev);
+    if (rc != NEOX_OK) return rc;
+    const float2* cs = nullptr;
+    if (rotary_dim > 0) {  // rows 0..127 (row factors) and every position < Smax
+      rc = get_table(device, std::max(Smax, neox::kRows), rotary_dim, rotary_base, stream, &cs);
+      if (rc != NEOX_OK) return rc;
+    }
+    CUtensorMap km, vm;
+    if ((rc = encode_cache_map(&km, k_cache, B, H, Smax, D)) != NEOX_OK) return rc;
+    if ((rc = encode_cache_map(&vm, v_cache, B, H, Smax, D)) != NEOX_OK) return rc;
+    // key-range splits: enough CTAs to keep every SM streaming (about four per SM)
+    const int tiles = (Smax + neox::kRows - 1) / neox::kRows;
+    const int64_t heads = static_cast<int64_t>(B) * H;
+    int splits = static_cast<int>(std::min<int64_t>(tiles, std::max<int64_t>(1, (4 * dev.num_sms + heads - 1) / heads)));
+    const int tps = (tiles + splits - 1) / splits;
+    splits = (tiles + tps - 1) / tps;
+    float* part = nullptr;
+    rc = get_scratch(device, static_cast<size_t>(heads) * splits * (D + 2) * sizeof(float), &part);
+    if (rc != NEOX_OK) return rc;
+    neox::DecodeParams p{};
+    p.qkv_new = static_cast<const uint16_t*>(qkv_new);
+    p.k_cache = static_cast<uint16_t*>(k_cache);
+    p.v_cache = static_cast<uint16_t*>(v_cache);
+    p.pos = pos;
+    p.cs = cs;
+    p.part = part;
+    p.out = static_cast<uint16_t*>(out);
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Smax = Smax;
+    p.r = rotary_dim;
+    p.splits = splits;
+    p.tiles_per_split = tps;
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    p.wait_limit_ns = neox::kWaitLimitNs;
+    const bool small = rotary_dim <= 32;
+    switch (D) {
+      case 64: return small ? launch_decode<64, true>(km, vm, p, stream) : launch_decode<64, false>(km, vm, p, stream);
+      case 96: return small ? launch_decode<96, true>(km, vm, p, stream) : launch_decode<96, false>(km, vm, p, stream);
+      default: return small ? launch_decode<128, true>(km, vm, p, stream) : launch_decode<128, false>(km, vm, p, stream);
+    }
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
+
 int neox_attn_get_device_error(void) {
   unsigned int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, neox::g_device_error, sizeof v);
@@ -287,7 +435,7 @@ int neox_attn_get_device_error(void) {
   const unsigned int zero = 0;
   e = cudaMemcpyToSymbol(neox::g_device_error, &zero, sizeof zero);
   if (e != cudaSuccess) return cuda_fail(e);
-  return NEOX_ERR_DEVICE_TIMEOUT;
+  return (v & neox::kErrTimeout) ? NEOX_ERR_DEVICE_TIMEOUT : NEOX_ERR_DEVICE_BAD_POSITION;
 }
 
 const char* neox_attn_status_string(int status) {
@@ -300,6 +448,7 @@ const char* neox_attn_status_string(int status) {
     case NEOX_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case NEOX_ERR_NO_DEVICE_SUPPORT: return "device is not compute capability 10.3";
     case NEOX_ERR_TOO_LARGE: return "S * rotary_dim/2 exceeds the fixed 1048576-entry table of neox_attn_fwd_noalloc";
+    case NEOX_ERR_DEVICE_BAD_POSITION: return "a decode position was outside [0, Smax)";
     default: return "unknown status";
   }
 }
@@ -318,6 +467,17 @@ void neox_attn_release(void) {
     }
     cudaSetDevice(cur);
     g_tables.clear();
+  }
+  if (!g_scratch.empty()) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& t : g_scratch) {
+      cudaSetDevice(t.device);
+      cudaDeviceSynchronize();
+      cudaFree(t.ptr);
+    }
+    cudaSetDevice(cur);
+    g_scratch.clear();
   }
 }
 

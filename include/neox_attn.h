@@ -45,7 +45,8 @@ typedef enum {
   NEOX_ERR_CUDA = -4,                 /* a CUDA runtime/driver call failed (see neox_attn_last_cuda_error) */
   NEOX_ERR_DEVICE_TIMEOUT = -5,       /* a kernel's bounded wait ran out; results are not valid */
   NEOX_ERR_NO_DEVICE_SUPPORT = -6,    /* current device is not compute capability 10.3 (B300) */
-  NEOX_ERR_TOO_LARGE = -7             /* neox_attn_fwd_noalloc: S * rotary_dim/2 > 1048576 */
+  NEOX_ERR_TOO_LARGE = -7,            /* neox_attn_fwd_noalloc: S * rotary_dim/2 > 1048576 */
+  NEOX_ERR_DEVICE_BAD_POSITION = -8   /* neox_attn_decode: a pos[b] was outside [0, Smax) */
 } neox_status;
 
 /*
@@ -116,9 +117,48 @@ int neox_attn_fwd_noalloc(const void* qkv, int B, int S, int H, int D, int rotar
                           void* out, float* lse, void* stream);
 
 /*
+ * Incremental decode: one new token per sequence against a key/value cache.
+ *
+ * GPT-NeoX serving runs a per-token decoder that extends a growing context
+ * ("GPT-NeoX on FasterTransformer" guide, section "背景"); the pages print no
+ * interface, so this one is the library's own.  Sequence b already holds pos[b]
+ * tokens; the new token sits at position pos[b].  Its query, rotated at pos[b],
+ * attends to keys 0..pos[b] (itself included), each rotated at its own position
+ * exactly as in neox_attn_fwd, scaled by 1/sqrt(D): the result equals row pos[b]
+ * of neox_attn_fwd over the whole sequence.  The new key and value are then part
+ * of the cache (row pos[b] is written).
+ *
+ *   qkv_new      device, bf16 [B, H, 3, D], contiguous (the new token's packed
+ *                projection, slot 0 = Q, 1 = K, 2 = V); 16-byte aligned; read only.
+ *   k_cache,     device, bf16 [B, H, Smax, D] each, contiguous, 16-byte aligned,
+ *   v_cache      not overlapping each other or any other argument.  Keys are stored
+ *                as projected, NOT rotated.  Rows p < pos[b] are read; row pos[b] is
+ *                overwritten with the new token's k / v (raw bf16, bit for bit);
+ *                rows > pos[b] are neither read nor written.
+ *   pos          device, int32 [B], 4-byte aligned: tokens already cached per
+ *                sequence, 0 <= pos[b] < Smax.  Read on the device only, so a value
+ *                out of range cannot be rejected before launch: that sequence's out
+ *                and lse are left undefined, its cache is not written, and
+ *                neox_attn_get_device_error() reports NEOX_ERR_DEVICE_BAD_POSITION.
+ *   B, H, Smax   each >= 1, B and H <= 65535, B*H*Smax*D < 2^40.
+ *   D, rotary_dim, rotary_base   as for neox_attn_fwd.
+ *   out          device, bf16 [B, H, D], 16-byte aligned, written.
+ *   lse          device, fp32 [B, H], 4-byte aligned, natural-log logsumexp.
+ *   stream       a cudaStream_t (NULL = legacy default stream).
+ *
+ * Ownership and errors as for neox_attn_fwd.  Besides the cos/sin table the library
+ * owns a per-device fp32 scratch buffer for the partial results of the key-range
+ * splits (grown on demand like the table; the call that grows it synchronizes the
+ * device once; neox_attn_release() frees it).
+ */
+int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const int* pos, int B, int H, int Smax,
+                     int D, int rotary_dim, float rotary_base, void* out, float* lse, void* stream);
+
+/*
  * Reads and clears the current device's error word written by the kernels' bounded
- * waits.  Call after synchronizing the streams that ran neox_attn_fwd.
- * Returns NEOX_OK, NEOX_ERR_DEVICE_TIMEOUT, or NEOX_ERR_CUDA if the read failed.
+ * waits and input checks.  Call after synchronizing the streams that ran the kernels.
+ * Returns NEOX_OK, NEOX_ERR_DEVICE_TIMEOUT, NEOX_ERR_DEVICE_BAD_POSITION (decode
+ * only), or NEOX_ERR_CUDA if the read failed.
  */
 int neox_attn_get_device_error(void);
 
@@ -128,8 +168,8 @@ const char* neox_attn_status_string(int status);
 /* The last CUDA error code the library saw on this host thread (0 = none). */
 int neox_attn_last_cuda_error(void);
 
-/* Frees the library-owned cos/sin tables on every device.  Waits for the device
- * first; not to be called while neox_attn_fwd work is being enqueued elsewhere. */
+/* Frees the library-owned cos/sin tables and decode scratch buffers on every device.
+ * Waits for the device first; not to be called while work is being enqueued elsewhere. */
 void neox_attn_release(void);
 
 /*

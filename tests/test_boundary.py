@@ -89,3 +89,36 @@ def test_torch_wrapper_rejects_cpu_tensors(lib):
     x = torch.zeros((1, 4, 1, 3, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         na.attn_fwd(x, 16)
+
+
+# ---- decode: neox_attn_decode(qkv_new, k_cache, v_cache, pos, B, H, Smax, D, r, base, out, lse)
+KC = 0x40000000
+VC = 0x50000000
+POS = 0x60000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, KC, VC, POS, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),    # null qkv_new
+    ((A, 0, VC, POS, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),     # null k_cache
+    ((A, KC, 0, POS, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),     # null v_cache
+    ((A, KC, VC, 0, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),      # null pos
+    ((A, KC, VC, POS, 2, 4, 256, 64, 16, 1e4, 0, LSE), na.NEOX_ERR_INVALID_ARG),      # null out
+    ((A, KC, VC, POS, 0, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),    # B = 0
+    ((A, KC, VC, POS, 2, 0, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),    # H = 0
+    ((A, KC, VC, POS, 2, 4, 0, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),      # Smax = 0
+    ((A, KC, VC, POS, 70000, 1, 16, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),  # B > 65535
+    ((A, KC, VC, POS, 2, 4, 256, 80, 16, 1e4, OUT, LSE), na.NEOX_ERR_UNSUPPORTED_HEAD_DIM),
+    ((A, KC, VC, POS, 2, 4, 256, 64, 15, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),    # odd rotary_dim
+    ((A, KC, VC, POS, 2, 4, 256, 64, 16, -1.0, OUT, LSE), na.NEOX_ERR_INVALID_ARG),   # base <= 0
+    ((A, KC + 8, VC, POS, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_MISALIGNED),  # k_cache 8-B aligned
+    ((A, KC, VC, POS + 2, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_MISALIGNED),  # pos 2-B aligned
+    ((A, KC, KC + 4096, POS, 2, 4, 256, 64, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),  # caches overlap
+    ((A, KC, VC, POS, 2, 4, 256, 64, 16, 1e4, KC + 64, LSE), na.NEOX_ERR_INVALID_ARG),  # out inside k_cache
+    ((A, KC, VC, POS, 1 << 10, 1 << 10, 1 << 20, 128, 16, 1e4, OUT, LSE), na.NEOX_ERR_INVALID_ARG),  # too large
+])
+def test_decode_invalid_arguments_rejected_before_cuda(lib, args, status):
+    assert na.neox_attn_decode(*args, stream=0) == status
+
+
+def test_decode_status_string(lib):
+    assert "position" in na.neox_attn_status_string(na.NEOX_ERR_DEVICE_BAD_POSITION)
