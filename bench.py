@@ -17,6 +17,10 @@ value is the FLOPs of all ranks over that time.
 
 --impl reference times the fp64 CPU oracle (the test oracle, as it stands) on the
 host cores on a bounded sample of the same workload per step; rank 0 only.
+
+--workload NAME-decode measures the incremental decode instead (neox_attn_decode: one
+new token per sequence against a resident K/V cache), in GB/s of cache read per step,
+against the measured HBM copy bandwidth (1 GPU).
 One JSON line on stdout (rank 0); everything else goes to stderr.
 """
 from __future__ import annotations
@@ -35,7 +39,8 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from causal_rope_self_neox_b300.workloads import WORKLOADS, bf16_bits, make_qkv  # noqa: E402
+from causal_rope_self_neox_b300.workloads import (DECODE_WORKLOADS, WORKLOADS, bf16_bits,  # noqa: E402
+                                                  make_decode_inputs, make_qkv)
 
 METRIC = "causal RoPE attention fwd TFLOP/s and % of B300 bf16 tensor peak"
 L2_FLUSH_BYTES = 256 << 20
@@ -384,18 +389,137 @@ def run_ours(args, w):
     return 0
 
 
+# ---------------------------------------------------------- decode workloads ----
+DECODE_METRIC = "incremental decode: KV-cache GB/s read per step (and tokens/s)"
+
+
+def run_decode(args, w):
+    """One step = one neox_attn_decode call: a new token for each of B sequences at
+    position pos against a cache of pos tokens (every cached key and value read once)."""
+    import torch
+    import causal_rope_self_neox_b300 as na
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    new_cpu, kc_cpu, vc_cpu = make_decode_inputs(w.B, w.H, w.Smax, w.D, w.seed)
+    new, kc, vc = new_cpu.to(dev), kc_cpu.to(dev), vc_cpu.to(dev)
+    pos_cpu = torch.full((w.B,), w.pos, dtype=torch.int32)
+    pos = pos_cpu.to(dev)
+    out = torch.empty((w.B, w.H, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(n=new, p_=pos):
+        rc = na.neox_attn_decode(n.data_ptr(), kc.data_ptr(), vc.data_ptr(), p_.data_ptr(), w.B, w.H, w.Smax, w.D,
+                                 w.rotary_dim, w.rotary_base, out.data_ptr(), lse.data_ptr(), sh)
+        if rc != 0:
+            raise na.NeoxAttnError(rc, "neox_attn_decode")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    na.check_device_error()
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = "0"
+    try:
+        u = str(props.uuid)
+        gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as cs:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    clocks = cs.summary()
+    na.check_device_error()
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_per_step = sum(ms) / len(ms)
+    # algorithmic bytes: cached K and V rows read, the new token's projections read, its
+    # k and v appended, out and lse written
+    alg_bytes = w.cache_bytes_read + w.B * w.H * 3 * w.D * 2 + w.B * w.H * w.D * 2 * 2 + w.B * w.H * w.D * 2 \
+        + w.B * w.H * 4
+    gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
+    # end to end: the new token's projections and positions in, out and lse back (the cache stays resident)
+    host_new, host_pos = new_cpu.pin_memory(), pos_cpu.pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dn, dp = torch.empty_like(new), torch.empty_like(pos)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dn.copy_(host_new, non_blocking=True)
+        dp.copy_(host_pos, non_blocking=True)
+        step(dn, dp)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    na.check_device_error()
+    _, _, hbm, src = load_peaks()
+    line = {
+        "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 caches and new tokens)",
+        "tokens_per_s": w.B / (ms_per_step / 1e3),
+        "config": {**w.describe(), "l2": "flushed before every step (256 MB write, outside the event interval)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "peak_kind": f"{src} HBM copy bandwidth",
+                     "kernel": f"attn_decode_kernel<D={w.D}> + combine",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "e2e": {"value": alg_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": host_new.numel() * 2 + host_pos.numel() * 4,
+                "d2h_bytes_per_step": host_out.numel() * 2 + host_lse.numel() * 4, "steps": e2e_steps,
+                "ms_per_step": e2e_ms,
+                "path": "pinned host new-token qkv + positions -> device, neox_attn_decode (C ABI), out + lse -> pinned host"},
+        "gpu_launches": 2 * args.steps,
+        "wall_s_timed_region": wall,
+        "kernel_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        nb_, kb, vb = bf16_bits(new_cpu), bf16_bits(kc_cpu), bf16_bits(vc_cpu)
+        used = oracle.default_threads()
+        t0 = time.perf_counter()
+        oracle.decode(nb_, kb, vb, [w.pos] * w.B, w.B, w.H, w.Smax, w.D, w.rotary_dim, w.rotary_base, used)
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": alg_bytes / secs / 1e9, "unit": "GB/s", "cores": used, "kind": "oracle",
+                                "seconds": secs,
+                                "sample": f"the whole step ({w.B * w.H} heads x {w.pos + 1} keys), fp64, {used} threads"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="neox20b")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS), default="neox20b")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload in DECODE_WORKLOADS:  # the decode path (a separate op, its own metric)
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "decode workloads have no reference arm"}))
+            return 0
+        return run_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

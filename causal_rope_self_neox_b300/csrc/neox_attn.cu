@@ -238,24 +238,6 @@ int get_scratch(int device, size_t bytes, float** out) {
   return NEOX_OK;
 }
 
-// A K or V cache [B, H, Smax, D] as 128-row x 32-column boxes with the 64-byte swizzle
-// (the prefill's tile layout); rows past Smax read as zeros.
-int encode_cache_map(CUtensorMap* map, const void* cache, int B, int H, int Smax, int D) {
-  CUtensorMap dummy;
-  int rc = encode_qkv_map(&dummy, cache, 1, 1, 1, D);  // resolves the driver entry point once
-  if (rc != NEOX_OK) return rc;
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Smax), static_cast<cuuint64_t>(H),
-                        static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Smax) * D * 2,
-                           static_cast<cuuint64_t>(H) * Smax * D * 2};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(neox::kBlkCols), static_cast<cuuint32_t>(neox::kRows), 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return res == CUDA_SUCCESS ? NEOX_OK : cuda_fail(cudaErrorInvalidValue);
-}
-
 int validate_decode(const void* qkv_new, const void* k_cache, const void* v_cache, const int* pos, int B, int H,
                     int Smax, int D, int r, float base, const void* out, const float* lse) {
   if (!qkv_new || !k_cache || !v_cache || !pos || !out || !lse) return NEOX_ERR_INVALID_ARG;
@@ -284,17 +266,30 @@ int validate_decode(const void* qkv_new, const void* k_cache, const void* v_cach
   return NEOX_OK;
 }
 
-template <int D, bool SMALL_R>
-int launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const neox::DecodeParams& p, cudaStream_t stream) {
+template <int D, int H2>
+int launch_decode_h2(const neox::DecodeParams& p, cudaStream_t stream) {
   const int smem = neox::dec_smem_bytes(D);
-  cudaError_t e = cudaFuncSetAttribute(neox::attn_decode_kernel<D, SMALL_R>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(neox::attn_decode_kernel<D, H2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  neox::attn_decode_kernel<D, SMALL_R><<<dim3(p.splits, p.H, p.B), neox::kDecThreads, smem, stream>>>(km, vm, p);
+  neox::attn_decode_kernel<D, H2><<<dim3(p.splits, p.H, p.B), neox::kDecThreads, smem, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   neox::attn_decode_combine_kernel<D><<<dim3(p.H, p.B), 128, 0, stream>>>(p);
   e = cudaGetLastError();
   return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
+}
+
+// rotary_dim 0, 8, 16, 24, 32: pairing fixed at compile time; others: the general path
+template <int D>
+int launch_decode(const neox::DecodeParams& p, int r, cudaStream_t stream) {
+  switch (r) {
+    case 0: return launch_decode_h2<D, 0>(p, stream);
+    case 8: return launch_decode_h2<D, 4>(p, stream);
+    case 16: return launch_decode_h2<D, 8>(p, stream);
+    case 24: return launch_decode_h2<D, 12>(p, stream);
+    case 32: return launch_decode_h2<D, 16>(p, stream);
+    default: return launch_decode_h2<D, -1>(p, stream);
+  }
 }
 
 __global__ void selftest_wait_kernel(uint64_t limit_ns) {
@@ -387,9 +382,6 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
       rc = get_table(device, std::max(Smax, neox::kRows), rotary_dim, rotary_base, stream, &cs);
       if (rc != NEOX_OK) return rc;
     }
-    CUtensorMap km, vm;
-    if ((rc = encode_cache_map(&km, k_cache, B, H, Smax, D)) != NEOX_OK) return rc;
-    if ((rc = encode_cache_map(&vm, v_cache, B, H, Smax, D)) != NEOX_OK) return rc;
     // key-range splits: enough CTAs to keep every SM streaming (about four per SM)
     const int tiles = (Smax + neox::kRows - 1) / neox::kRows;
     const int64_t heads = static_cast<int64_t>(B) * H;
@@ -416,11 +408,10 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
     p.tiles_per_split = tps;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
-    const bool small = rotary_dim <= 32;
     switch (D) {
-      case 64: return small ? launch_decode<64, true>(km, vm, p, stream) : launch_decode<64, false>(km, vm, p, stream);
-      case 96: return small ? launch_decode<96, true>(km, vm, p, stream) : launch_decode<96, false>(km, vm, p, stream);
-      default: return small ? launch_decode<128, true>(km, vm, p, stream) : launch_decode<128, false>(km, vm, p, stream);
+      case 64: return launch_decode<64>(p, rotary_dim, stream);
+      case 96: return launch_decode<96>(p, rotary_dim, stream);
+      default: return launch_decode<128>(p, rotary_dim, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
