@@ -26,7 +26,6 @@ One JSON line on stdout (rank 0); everything else goes to stderr.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -64,10 +63,13 @@ def load_peaks():
         return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
 
 
+FWD_KERNEL_SOURCES = ("attn_ws.cuh", "attn_common.cuh", "ptx.cuh", "rotary.cuh", "tile_layout.cuh")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the sources the prefill kernel is compiled from (not the decode path)."""
     h = hashlib.sha256()
-    files = sorted(glob.glob(os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", "*"))) + \
-        sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
+    files = [os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", n) for n in FWD_KERNEL_SOURCES]
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())

@@ -382,7 +382,8 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
       rc = get_table(device, std::max(Smax, neox::kRows), rotary_dim, rotary_base, stream, &cs);
       if (rc != NEOX_OK) return rc;
     }
-    // key-range splits: enough CTAs to keep every SM streaming (about four per SM)
+    // key-range splits: about four CTAs per SM in total (one runs at a time); each CTA
+    // costs a start-up and a reduction, so a head is split only when there are few heads
     const int tiles = (Smax + neox::kRows - 1) / neox::kRows;
     const int64_t heads = static_cast<int64_t>(B) * H;
     int splits = static_cast<int>(std::min<int64_t>(tiles, std::max<int64_t>(1, (4 * dev.num_sms + heads - 1) / heads)));
