@@ -9,21 +9,28 @@
 //
 // One query per head makes this a matrix-vector product: HBM-bound (every cached key and
 // value is read once), so the tensor cores have no part in it.  Layout of the work:
-//   attn_decode_kernel: CTA (split, h, b) streams 128-key tiles [t0, t1) of its head's
-//     K and V through a shared-memory ring: a head's cache rows are contiguous, so each
-//     tile is one bulk copy per operand (row-major [128][D] in shared memory, rows past
-//     Smax not copied).  Warp 0 issues the copies; 256 consumer threads
-//     work in pairs on the key rows of every tile, each thread owning half of the head
-//     dims: rotate, partial score (four independent FMA chains), pair sum, online
-//     softmax, accumulate p * v for its dims in registers.  The CTA then reduces its 128
-//     partial states and writes (m, l, o[D]) for its split.
-//   attn_decode_combine_kernel: merges the splits of a head into out (bf16) and lse.
-// Rotation: dims i < r/2 pair with i + r/2.  For r <= 32 the angle of key p = 128 t + row
-// comes from angle addition, (cos, sin)(p w) = (cos, sin)(128 t w) x (cos, sin)(row w),
-// with the row factor held in registers and the tile factor read once per tile (both are
-// table entries, fp64-computed and stored fp32; the product is within ~3e-7 of the exact
-// value, far below the 2^-9 of the bf16 inputs); for larger r each key reads its own
-// table row.
+//   attn_decode_kernel: persistent, one CTA per SM.  The B*H*ceil(Smax/128) key tiles of
+//     all heads, taken head after head, are cut into one contiguous range per CTA (equal
+//     to within one tile, whatever B, H and Smax are); the run of a range inside one head
+//     is a work item whose partial softmax state (m, l, o[D]) goes to a scratch slot.
+//     Warp 0 streams the items' K and V tiles (one bulk copy per operand: a head's cache
+//     rows are contiguous) through a shared-memory ring that runs on across items, and
+//     each item's new-token row (q, k, v) and query angle into one of two item slots.
+//     Warps 1-8 form 32 row groups of 8 lanes; group g takes rows g, g+32, g+64, g+96 of
+//     every tile, and lane l of a group owns D/8 dims of the row (16-byte chunk l, plus
+//     chunk l+8 for D = 128 or the 8-byte piece l of dims 64..95 for D = 96), so the 8
+//     lanes reading one row touch 8 distinct bank groups.  Partial dot products meet in
+//     three shuffles; each group keeps its own online softmax; at the end of an item the
+//     groups merge by shuffles inside a warp and through shared memory across warps.
+//   attn_decode_combine_kernel: merges the partial states of a head into out and lse.
+// Rotation, with the cache keys unrotated: for pair (i, i + r/2) and key angle phi,
+//   q'_i k'_i + q'_{i+r/2} k'_{i+r/2} = k_i Re(z e^{-j phi}) + k_{i+r/2} Im(z e^{-j phi}),
+// z = q'_i + j q'_{i+r/2}, so the query is turned instead of the key.  For r = 8..32 all
+// rotated dims sit in chunk 0 of lanes 0..r/8-1, and e^{-j phi} of key 128 t + row splits
+// into a tile factor (applied to z once per tile) and a row factor (held in registers:
+// each lane sees the same 4 rows in every tile); the product of the two fp32 table entries
+// is within ~3e-7 of the exact value, far below the 2^-9 of the bf16 inputs.  Other r
+// read each key's angle from the table.
 #pragma once
 
 #include "attn_common.cuh"
@@ -35,326 +42,452 @@ struct DecodeParams {
   uint16_t* k_cache;        // bf16 [B, H, Smax, D]
   uint16_t* v_cache;
   const int* pos;           // int32 [B]
-  const float2* cs;         // cos/sin table [>= Smax rows][r/2]
-  float* part;              // fp32 [B, H, splits, D + 2]: o[D], m, l  (m in log2 units)
+  const float2* cs;         // cos/sin table [max(Smax, 128) rows][r/2]
+  float* part;              // fp32 [B*H][runs_per_head][D + 2]: o[D], m, l  (m in log2 units)
   uint16_t* out;            // bf16 [B, H, D]
   float* lse;               // fp32 [B, H]
   int B, H, Smax, r;
-  int splits, tiles_per_split;
+  int tiles_per_head;       // ceil(Smax / 128)
+  int runs_per_head;        // partial-state slots per head (CTAs one head's tiles can span)
+  long long total_tiles;    // B * H * tiles_per_head
   float scale_log2;         // log2(e) / sqrt(D)
   uint64_t wait_limit_ns;
 };
 
-constexpr int kDecThreads = 288;  // warp 0: TMA; warps 1-8: two threads per key row
-// One CTA per SM (registers), with a deep ring: 4 stages of K + V tiles (3 for D = 128),
-// 192 KB of loads in flight.
-__host__ __device__ constexpr int dec_stages(int D) { return D == 128 ? 3 : 4; }
-constexpr int kDecMaxStages = 4;
-
-__host__ __device__ constexpr int dec_tile_bytes(int D) { return tile_bytes(D); }
-// smem: stages x (K tile + V tile), q' (fp32 D), per stage the tile's angle factor (16
-// float2), barriers; the tiles double as the reduction buffer [D][128] fp32 at the end
-// (D * 512 bytes <= stages x 2 tiles).
+constexpr int kDecThreads = 288;  // warp 0: copies; warps 1-8: 32 row groups of 8 lanes
+constexpr int kDecRingBytes = 192 * 1024;
+// ring stages of K + V tiles in 192 KB: 6 (D = 64), 4 (D = 96), 3 (D = 128)
+__host__ __device__ constexpr int dec_stages(int D) { return kDecRingBytes / (2 * tile_bytes(D)); }
+__host__ __device__ constexpr int dec_slot_bytes(int D) { return 3 * D * 2 + 16 * 8; }  // q|k|v, query angle
+// smem: ring, 2 item slots, per stage the tile factor (16 float2 + the identity), the
+// cross-warp merge buffer [2][8][D + 2], barriers, abort flag and the slots' positions
 __host__ __device__ constexpr int dec_smem_bytes(int D) {
-  return dec_stages(D) * 2 * dec_tile_bytes(D) + D * 4 + kDecMaxStages * 16 * 8 + 2 * kDecMaxStages * 8 + 16 + 512;
+  return kDecRingBytes + 2 * dec_slot_bytes(D) + dec_stages(D) * 18 * 8 + 2 * 8 * (D + 2) * 4 +
+         (2 * dec_stages(D) + 4) * 8 + 16 + 512;
+}
+
+// The CTA whose tile range holds global tile x (ranges [N c / G, N (c + 1) / G)).
+__host__ __device__ __forceinline__ long long dec_cta_of(long long x, long long N, int G) {
+  return ((x + 1) * G - 1) / N;
 }
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-// dim e (0..31) of four 8-dim chunks held in registers (e a compile-time constant after
-// unrolling: no address is taken, so the chunks stay in registers)
-__device__ __forceinline__ float dim_of(const uint4 (&k)[4], int e) {
-  const uint4& c = k[e >> 3];
-  const int q = (e & 7) >> 1;
-  const uint32_t w = q == 0 ? c.x : q == 1 ? c.y : q == 2 ? c.z : c.w;
-  return (e & 1) ? bf16hi(w) : bf16lo(w);
-}
-__device__ __forceinline__ float dim_of(const uint4& c, int e) {  // dim e (0..7) of one chunk
-  const int q = e >> 1;
-  const uint32_t w = q == 0 ? c.x : q == 1 ? c.y : q == 2 ? c.z : c.w;
-  return (e & 1) ? bf16hi(w) : bf16lo(w);
+__device__ __forceinline__ float word_dim(uint32_t w, int odd) { return odd ? bf16hi(w) : bf16lo(w); }
+
+// The D/8 dims lane l8 of a row group owns: v < 8 -> 8 l8 + v (chunk l8); v >= 8 ->
+// 64 + 8 l8 + (v - 8) (chunk l8 + 8, D = 128) or 64 + 4 l8 + (v - 8) (piece l8, D = 96).
+template <int D>
+__device__ __forceinline__ int lane_dim(int l8, int v) {
+  return v < 8 ? 8 * l8 + v : (D == 128 ? 64 + 8 * l8 + (v - 8) : 64 + 4 * l8 + (v - 8));
 }
 
-// H2 = rotary_dim / 2 when it is 0, 4, 8, 12 or 16 (compile-time pairing, angle addition),
-// or -1 for any other rotary_dim (runtime pairing, one table row per key).
+// One row's share of a lane, as loaded from a row-major [*][D] bf16 row in shared memory.
+template <int D>
+struct LaneRow {
+  uint4 c0;
+  uint4 c1;  // D = 128
+  uint2 pc;  // D = 96
+  __device__ __forceinline__ void load(const uint8_t* row, int l8) {
+    c0 = *reinterpret_cast<const uint4*>(row + 16 * l8);
+    if constexpr (D == 128) c1 = *reinterpret_cast<const uint4*>(row + 128 + 16 * l8);
+    if constexpr (D == 96) pc = *reinterpret_cast<const uint2*>(row + 128 + 8 * l8);
+  }
+  // dim v of the lane (v a compile-time constant after unrolling)
+  __device__ __forceinline__ float at(int v) const {
+    if (v < 8) {
+      const int q = (v & 7) >> 1;
+      return word_dim(q == 0 ? c0.x : q == 1 ? c0.y : q == 2 ? c0.z : c0.w, v & 1);
+    }
+    if constexpr (D == 128) {
+      const int q = (v & 7) >> 1;
+      return word_dim(q == 0 ? c1.x : q == 1 ? c1.y : q == 2 ? c1.z : c1.w, v & 1);
+    }
+    return word_dim(((v - 8) >> 1) == 0 ? pc.x : pc.y, v & 1);
+  }
+};
+
+// Named barrier over the 256 consumer threads that also ORs a flag across them.
+__device__ __forceinline__ bool consumers_sync_or(bool flag) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, 1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(res)
+      : "r"(static_cast<uint32_t>(flag))
+      : "memory");
+  return res != 0;
+}
+
+// H2 = rotary_dim / 2 when it is 0, 4, 8, 12 or 16 (tile x row factorisation of the
+// angle), or -1 for any other rotary_dim (one table read per key and rotated dim).
 template <int D, int H2>
 __global__ void __launch_bounds__(kDecThreads, 1)
     attn_decode_kernel(const DecodeParams p) {
   constexpr bool SMALL_R = H2 >= 0;
+  constexpr int NV = D / 8;  // dims per lane
+  constexpr int S = dec_stages(D);
+  constexpr int TB = tile_bytes(D);
+  constexpr int SLOT = dec_slot_bytes(D);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 511) & ~uintptr_t(511));
-  constexpr int TB = dec_tile_bytes(D);
-  constexpr int kDecStages = dec_stages(D);
-  float* qs = reinterpret_cast<float*>(smem + kDecStages * 2 * TB);  // q' scaled by log2(e)/sqrt(D)
-  float2* tf = reinterpret_cast<float2*>(qs + D);                      // [stages][16] angle of 128 t
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tf + kDecStages * 16);  // full[stages], empty[stages]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kDecStages);
+  uint8_t* slots = smem + kDecRingBytes;                                  // [2][SLOT]
+  float2* tf = reinterpret_cast<float2*>(slots + 2 * SLOT);              // [S][18]
+  float* red = reinterpret_cast<float*>(tf + S * 18);                    // [2][8][D + 2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 2 * 8 * (D + 2));   // full, empty, qfull, qempty
+  int* misc = reinterpret_cast<int*>(bars + 2 * S + 4);                  // abort flag, slot positions
+  volatile int* abort_flag = misc;
+  int* slot_pos = misc + 1;
   auto full = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty = [&](int s) { return smem_u32(&bars[kDecStages + s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[S + s]); };
+  auto qfull = [&](int i) { return smem_u32(&bars[2 * S + i]); };
+  auto qempty = [&](int i) { return smem_u32(&bars[2 * S + 2 + i]); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int h2 = SMALL_R ? H2 : (p.r >> 1);
   const uint64_t lim = p.wait_limit_ns;
-
-  const int P = p.pos[b];
-  const bool pos_ok = P >= 0 && P < p.Smax;
-  const int n_tiles = pos_ok ? P / kRows + 1 : 0;
-  const int t0 = split * p.tiles_per_split;
-  const int t1 = min(t0 + p.tiles_per_split, n_tiles);
-  float* part = p.part + ((static_cast<int64_t>(b) * p.H + h) * p.splits + split) * (D + 2);
-  if (!pos_ok && split == 0 && tid == 0) record_error(kErrBadInput, 0);
-  if (t0 >= t1) {  // nothing to do for this split: an empty partial state
-    for (int d = tid; d < D; d += kDecThreads) part[d] = 0.0f;
-    if (tid == 0) {
-      part[D] = -INFINITY;
-      part[D + 1] = 0.0f;
-    }
-    return;
-  }
+  const int G = gridDim.x, cta = blockIdx.x;
+  const long long N = p.total_tiles;
+  const long long lo = N * cta / G, hi = N * (cta + 1) / G;
+  const int Th = p.tiles_per_head;
 
   if (tid == 0) {
-    for (int s = 0; s < kDecStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 256);
+      mbar_init(empty(s), 8);
+      tf[s * 18 + 16] = make_float2(1.0f, 0.0f);  // identity factor for unrotated dims
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(qfull(i), 1);
+      mbar_init(qempty(i), 8);
     }
     *abort_flag = 0;
     fence_barrier_init();
-  }
-  // q' = rotate(q_new, P) * log2(e)/sqrt(D), by the consumer threads
-  const uint16_t* qn = p.qkv_new + (static_cast<int64_t>(b) * p.H + h) * 3 * D;
-  if (tid >= 32) {
-    const int d = tid - 32;
-    if (d < h2) {
-      const float2 c = p.cs[static_cast<int64_t>(P) * h2 + d];
-      const float x1 = bf16_bits_to_f32(qn[d]), x2 = bf16_bits_to_f32(qn[d + h2]);
-      qs[d] = (x1 * c.x - x2 * c.y) * p.scale_log2;
-      qs[d + h2] = (x2 * c.x + x1 * c.y) * p.scale_log2;
-    }
-    if (p.r + d < D) qs[p.r + d] = bf16_bits_to_f32(qn[p.r + d]) * p.scale_log2;
   }
   __syncthreads();
 
   if (warp == 0) {
     // ================================================================ producer ====
-    if (lane == 0) {
-      bool ok = true;
-      int armed = 0;  // bitmask of stages with a load in flight, and their parities
-      uint32_t par_bits = 0;
-      for (int t = t0; t < t1 && ok; ++t) {
-        const int s = (t - t0) % kDecStages;
-        const uint32_t lap = static_cast<uint32_t>((t - t0) / kDecStages) & 1u;
-        if (!wait_phase(empty(s), lap ^ 1, abort_flag, lim, 50)) { ok = false; break; }
-        const int rows = min(kRows, p.Smax - t * kRows);  // never past the head's last row
-        const uint32_t bytes = static_cast<uint32_t>(rows) * D * 2;
-        if (SMALL_R)  // the tile's angle factor, published with the arrival below
-          for (int i = 0; i < h2; ++i) tf[s * 16 + i] = p.cs[static_cast<int64_t>(t) * kRows * h2 + i];
-        mbar_arrive_expect_tx(full(s), 2 * bytes);
-        armed |= 1 << s;
-        par_bits = (par_bits & ~(1u << s)) | (lap << s);
-        const int64_t row0 = (static_cast<int64_t>(b) * p.H + h) * p.Smax + static_cast<int64_t>(t) * kRows;
-        bulk_load(smem_u32(smem + (2 * s) * TB), p.k_cache + row0 * D, bytes, full(s));
-        bulk_load(smem_u32(smem + (2 * s + 1) * TB), p.v_cache + row0 * D, bytes, full(s));
+    bool ok = true;
+    uint32_t armed = 0, par_bits = 0, qarmed = 0, qpar_bits = 0;
+    uint32_t n = 0;  // tiles issued by this CTA
+    int k = 0;       // items
+    for (long long g = lo; g < hi && ok; ++k) {
+      const long long head = g / Th;
+      const int tb = static_cast<int>(g - head * Th);
+      const long long gend = min(hi, (head + 1) * Th);
+      const int te = tb + static_cast<int>(gend - g);
+      g = gend;
+      const int b = static_cast<int>(head / p.H);
+      const int P = p.pos[b];
+      const bool valid = P >= 0 && P < p.Smax;
+      if (!valid && tb == 0 && lane == 0) record_error(kErrBadInput, 0);
+      const int t1 = min(te, valid ? P / kRows + 1 : 0);
+      const int slot = k & 1;
+      const uint32_t qlap = static_cast<uint32_t>(k >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, wait_phase(qempty(slot), qlap ^ 1, abort_flag, lim, 52))) {
+        ok = false;
+        break;
       }
-      if (!ok || *abort_flag)
-        for (int s = 0; s < kDecStages; ++s)
-          if (armed & (1 << s)) drain_phase(full(s), (par_bits >> s) & 1, lim);
+      if (lane == 0) {
+        slot_pos[slot] = P;  // published by the arrival below
+        const bool tab = SMALL_R && H2 > 0 && valid;
+        constexpr uint32_t kAngBytes = (SMALL_R ? H2 : 0) * 8;
+        mbar_arrive_expect_tx(qfull(slot), 3 * D * 2 + (tab ? kAngBytes : 0));
+        bulk_load(smem_u32(slots + slot * SLOT), p.qkv_new + head * 3 * D, 3 * D * 2, qfull(slot));
+        if (tab)
+          bulk_load(smem_u32(slots + slot * SLOT + 6 * D), p.cs + static_cast<long long>(P) * (SMALL_R ? H2 : 0),
+                    kAngBytes, qfull(slot));
+      }
+      qarmed |= 1u << slot;
+      qpar_bits = (qpar_bits & ~(1u << slot)) | (qlap << slot);
+      for (int t = tb; t < t1; ++t, ++n) {
+        const int s = static_cast<int>(n % S);
+        const uint32_t lap = (n / S) & 1u;
+        float2 fac = make_float2(1.0f, 0.0f);
+        if (SMALL_R && lane < H2) fac = p.cs[static_cast<long long>(t) * kRows * (SMALL_R ? H2 : 0) + lane];
+        if (!__all_sync(0xffffffffu, wait_phase(empty(s), lap ^ 1, abort_flag, lim, 50))) {
+          ok = false;
+          break;
+        }
+        if (SMALL_R && lane < H2) tf[s * 18 + lane] = fac;  // the tile factor, published below
+        __syncwarp();
+        if (lane == 0) {
+          const int rows = min(kRows, p.Smax - t * kRows);  // never past the head's last row
+          const uint32_t bytes = static_cast<uint32_t>(rows) * D * 2;
+          mbar_arrive_expect_tx(full(s), 2 * bytes);
+          const long long row0 = head * p.Smax + static_cast<long long>(t) * kRows;
+          bulk_load(smem_u32(smem + (2 * s) * TB), p.k_cache + row0 * D, bytes, full(s));
+          bulk_load(smem_u32(smem + (2 * s + 1) * TB), p.v_cache + row0 * D, bytes, full(s));
+        }
+        armed |= 1u << s;
+        par_bits = (par_bits & ~(1u << s)) | (lap << s);
+      }
+    }
+    if (lane == 0 && (!ok || *abort_flag)) {  // let every copy in flight land before exit
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) drain_phase(full(s), (par_bits >> s) & 1, lim);
+      for (int i = 0; i < 2; ++i)
+        if (qarmed & (1u << i)) drain_phase(qfull(i), (qpar_bits >> i) & 1, lim);
     }
     __syncwarp();
   } else {
     // =============================================================== consumers ====
-    constexpr int DH = D / 2;           // output dims per thread
-    const int c = tid - 32;             // 0..255
-    const int row = c >> 1, half = c & 1;  // key row of every tile; which half of the dims
-    // score dims: half 0 takes the rotated dims [0, r) and pass-through chunks up to `mid`,
-    // half 1 the pass-through chunks from `mid` (8-dim chunks; r is even)
-    const int r8 = p.r >> 3;  // first chunk holding a pass-through dim
-    const int mid8 = r8 + (D / 8 - r8) / 2;
-    const int cb0 = half == 0 ? r8 : mid8, cb1 = half == 0 ? mid8 : D / 8;
-    // row factor of the rotation angle: (cos, sin)(row * w_i), i < r/2 (r <= 32, half 0)
-    float2 off[SMALL_R && H2 > 0 ? H2 : 1];
-    if constexpr (SMALL_R) {
+    const int cw = warp - 1;                  // consumer warp 0..7
+    const int l8 = lane & 7;                  // lane of the row group
+    const int grp = cw * 4 + (lane >> 3);     // row group: rows grp + 32 jj of every tile
+    const int h2 = SMALL_R ? H2 : (p.r >> 1);
+    // lanes whose chunk 0 holds rotated dims (r = 8..32: chunks 0..r/8-1, all 8 dims)
+    const bool rot_lane = SMALL_R && 8 * l8 < 2 * h2;
+    // pair index of chunk-0 dim v, or 16 (the identity factor) on unrotated lanes
+    auto pair0 = [&](int v) { return rot_lane ? (8 * l8 + v < h2 ? 8 * l8 + v : 8 * l8 + v - h2) : 16; };
+    auto is_a0 = [&](int v) { return !rot_lane || 8 * l8 + v < h2; };  // first half of its pair
+    // row factors e^{j row w}: (cos, sin)(row w_pair) for rows grp + 32 jj
+    float cr[4][8], sr[4][8];
+    if constexpr (SMALL_R && H2 > 0) {
 #pragma unroll
-      for (int i = 0; i < H2; ++i) off[i] = half == 0 ? p.cs[static_cast<int64_t>(row) * H2 + i] : make_float2(1.f, 0.f);
+      for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float2 f = rot_lane ? p.cs[(grp + 32 * jj) * H2 + pair0(v)] : make_float2(1.0f, 0.0f);
+          cr[jj][v] = f.x;
+          sr[jj][v] = f.y;
+        }
     }
-    float m = -INFINITY, l = 0.0f;
-    float o[DH];
+    uint32_t n = 0;
+    int k = 0;
+    for (long long g = lo; g < hi; ++k) {
+      const long long head = g / Th;
+      const int tb = static_cast<int>(g - head * Th);
+      const long long gend = min(hi, (head + 1) * Th);
+      const int te = tb + static_cast<int>(gend - g);
+      g = gend;
+      const int slot = k & 1;
+      const uint32_t qlap = static_cast<uint32_t>(k >> 1) & 1u;
+      bool ok = __all_sync(0xffffffffu, wait_phase(qfull(slot), qlap, abort_flag, lim, 53));
+      const int P = ok ? slot_pos[slot] : -1;
+      const bool valid = P >= 0 && P < p.Smax;
+      const int t1 = min(te, valid ? P / kRows + 1 : 0);
+      const uint16_t* sq = reinterpret_cast<const uint16_t*>(slots + slot * SLOT);  // q | k | v
+      const float2* sang = reinterpret_cast<const float2*>(slots + slot * SLOT + 6 * D);
+      // the lane's query dims, rotated at P and scaled by log2(e)/sqrt(D): z = (q'_i, q'_{i+h2})
+      // of each rotated dim's pair; q'_d (and 0) for the others
+      float zr[NV], zi[NV];
 #pragma unroll
-    for (int d = 0; d < DH; ++d) o[d] = 0.0f;
-    const uint16_t* kn = qn + D;
-    const uint16_t* vn = qn + 2 * D;
-    const float4* q4 = reinterpret_cast<const float4*>(qs);
-    for (int t = t0; t < t1; ++t) {
-      const int s = (t - t0) % kDecStages;
-      const uint32_t lap = static_cast<uint32_t>((t - t0) / kDecStages) & 1u;
-      // warp-uniform exit: the pair sum below is a warp-synchronous shuffle
-      if (!__all_sync(0xffffffffu, wait_phase(full(s), lap, abort_flag, lim, 51))) break;
-      const uint8_t* kt = smem + (2 * s) * TB;
-      const uint8_t* vt = smem + (2 * s + 1) * TB;
-      const int key = t * kRows + row;
-      // lanes with a key in range (both threads of a pair agree): the shuffle's members
-      const unsigned active = __ballot_sync(0xffffffffu, key <= P);
-      if (key <= P) {
-        const bool is_new = key == P;
-        auto kchunk = [&](int c8) -> uint4 {  // dims [8 c8, 8 c8 + 8) of the key
-          return is_new ? reinterpret_cast<const uint4*>(kn)[c8]
-                        : reinterpret_cast<const uint4*>(kt + row * (2 * D))[c8];
-        };
-        float sa = 0.0f, sb = 0.0f, sc2 = 0.0f, sd = 0.0f;  // four independent chains
-        if (half == 0 && h2 > 0) {
-          if constexpr (SMALL_R) {
-            const float2* tb = tf + s * 16;  // angle of 128 t
-            uint4 kc[4];
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) kc[c8] = c8 * 8 < 2 * H2 ? kchunk(c8) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < H2; ++i) {
-              {
-                const float2 bt = tb[i];
-                const float cth = bt.x * off[i].x - bt.y * off[i].y, sth = bt.y * off[i].x + bt.x * off[i].y;
-                const int j2 = i + H2;
-                const float x1 = dim_of(kc, i), x2 = dim_of(kc, j2);
-                if (i & 1) {
-                  sa = fmaf(qs[i], x1 * cth - x2 * sth, sa);
-                  sb = fmaf(qs[j2], x2 * cth + x1 * sth, sb);
-                } else {
-                  sc2 = fmaf(qs[i], x1 * cth - x2 * sth, sc2);
-                  sd = fmaf(qs[j2], x2 * cth + x1 * sth, sd);
-                }
-              }
-            }
-          } else {
-            const float2* cr = p.cs + static_cast<int64_t>(key) * h2;
-            for (int i = 0; i < h2; ++i) {
-              const float2 cs = cr[i];
-              const int j2 = i + h2;
-              const uint4 ci = kchunk(i >> 3), cj = kchunk(j2 >> 3);
-              const int ei = i & 7, ej = j2 & 7;
-              float x1 = 0.0f, x2 = 0.0f;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                if (e == ei) x1 = dim_of(ci, e);
-                if (e == ej) x2 = dim_of(cj, e);
-              }
-              sa = fmaf(qs[i], x1 * cs.x - x2 * cs.y, sa);
-              sb = fmaf(qs[j2], x2 * cs.x + x1 * cs.y, sb);
-            }
-          }
-        }
-        // pass-through dims of this half, a chunk at a time
-        for (int c8 = cb0; c8 < cb1; ++c8) {
-          const uint4 kc = kchunk(c8);
-          const float4 qa = q4[2 * c8], qb = q4[2 * c8 + 1];
-          const int d0 = 8 * c8;
-          if (d0 >= p.r) {
-            sa = fmaf(qa.x, bf16lo(kc.x), sa);
-            sb = fmaf(qa.y, bf16hi(kc.x), sb);
-            sc2 = fmaf(qa.z, bf16lo(kc.y), sc2);
-            sd = fmaf(qa.w, bf16hi(kc.y), sd);
-            sa = fmaf(qb.x, bf16lo(kc.z), sa);
-            sb = fmaf(qb.y, bf16hi(kc.z), sb);
-            sc2 = fmaf(qb.z, bf16lo(kc.w), sc2);
-            sd = fmaf(qb.w, bf16hi(kc.w), sd);
-          } else {  // the chunk holding dim r: only its dims >= r
-            const float qv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (d0 + e >= p.r) sa = fmaf(qv[e], dim_of(kc, e), sa);
-          }
-        }
-        float sc = (sa + sb) + (sc2 + sd);
-        sc += __shfl_xor_sync(active, sc, 1);  // the pair's two halves
-        // online softmax of this pair's keys (log2 units), lazy rescale beyond 2^8
-        if (sc > m + 8.0f || m == -INFINITY) {
-          const float mn = fmaxf(sc, m);
-          const float f = ex2_approx(m - mn);
-          l *= f;
-#pragma unroll
-          for (int d = 0; d < DH; ++d) o[d] *= f;
-          m = mn;
-        }
-        const float pw = ex2_approx(sc - m);
-        l += pw;
-#pragma unroll
-        for (int c8 = 0; c8 < DH / 8; ++c8) {
-          const int cv = half * (DH / 8) + c8;
-          const uint4 vc = is_new ? reinterpret_cast<const uint4*>(vn)[cv]
-                                  : reinterpret_cast<const uint4*>(vt + row * (2 * D))[cv];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[8 * c8 + e] = fmaf(pw, dim_of(vc, e), o[8 * c8 + e]);
-        }
-        if (is_new) {  // append the new token's raw key and value (its tile has landed)
-          uint4* kd = reinterpret_cast<uint4*>(p.k_cache + ((static_cast<int64_t>(b) * p.H + h) * p.Smax + P) * D);
-          uint4* vd = reinterpret_cast<uint4*>(p.v_cache + ((static_cast<int64_t>(b) * p.H + h) * p.Smax + P) * D);
-#pragma unroll
-          for (int c8 = half * (D / 16); c8 < (half + 1) * (D / 16); ++c8) {
-            kd[c8] = reinterpret_cast<const uint4*>(kn)[c8];
-            vd[c8] = reinterpret_cast<const uint4*>(vn)[c8];
-          }
+      for (int v = 0; v < NV; ++v) {
+        const int d = lane_dim<D>(l8, v);
+        zr[v] = bf16_bits_to_f32(sq[d]) * p.scale_log2;
+        zi[v] = 0.0f;
+        const bool rot = SMALL_R ? (v < 8 && rot_lane) : d < p.r;
+        if (rot && valid) {
+          const int i = d < h2 ? d : d - h2;
+          const float2 c = SMALL_R ? sang[i] : p.cs[static_cast<long long>(P) * h2 + i];
+          const float x1 = bf16_bits_to_f32(sq[i]), x2 = bf16_bits_to_f32(sq[i + h2]);
+          zr[v] = (x1 * c.x - x2 * c.y) * p.scale_log2;
+          zi[v] = (x2 * c.x + x1 * c.y) * p.scale_log2;
         }
       }
-      mbar_arrive(empty(s));  // this thread is done with stage s
-    }
-    // ---- CTA reduction of the 128 partial states -> (o, m, l) of this split
-    // (the ring becomes the [D][128] buffer once every consumer has passed its last
-    // tile, which the first barrier below ensures)
-    float* red = reinterpret_cast<float*>(smem);
-    float* mred = qs;  // 8 warp maxima, then 8 warp sums (q' is dead after the barrier)
-    float wm = m;
+      float m = -INFINITY, l = 0.0f;
+      float o[NV];
 #pragma unroll
-    for (int k = 16; k > 0; k >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, k));
-    asm volatile("bar.sync 1, 256;" ::: "memory");  // consumers only: every tile consumed
-    if (lane == 0) mred[warp - 1] = wm;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    float M = mred[0];
+      for (int v = 0; v < NV; ++v) o[v] = 0.0f;
+
+      for (int t = tb; ok && t < t1; ++t, ++n) {
+        const int s = static_cast<int>(n % S);
+        const uint32_t lap = (n / S) & 1u;
+        if (!__all_sync(0xffffffffu, wait_phase(full(s), lap, abort_flag, lim, 51))) {
+          ok = false;
+          break;
+        }
+        // chunk-0 coefficients of this tile: w = z e^{-j 128 t w}; dim i of a pair takes
+        // Re(w e^{-j row w}) = wr c + wi s, dim i + h2 takes Im(...) = wi c - wr s
+        float ca[8], cb[8];
+        if constexpr (SMALL_R && H2 > 0) {
 #pragma unroll
-    for (int w = 1; w < 8; ++w) M = fmaxf(M, mred[w]);
-    const float f = (m == -INFINITY) ? 0.0f : ex2_approx(m - M);
-    float lf = half == 0 ? l * f : 0.0f;  // each key's l counted once
+          for (int v = 0; v < 8; ++v) {
+            const float2 f = tf[s * 18 + pair0(v)];
+            const float wr = zr[v] * f.x + zi[v] * f.y, wi = zi[v] * f.x - zr[v] * f.y;
+            ca[v] = is_a0(v) ? wr : wi;
+            cb[v] = is_a0(v) ? wi : -wr;
+          }
+        }
+        const uint8_t* kt = smem + (2 * s) * TB;
+        const uint8_t* vt = kt + TB;
+        const bool whole = t * kRows + kRows - 1 < P;  // every row valid, none is the new token
+        float sc[4];
+        LaneRow<D> kr[4];
 #pragma unroll
-    for (int k = 16; k > 0; k >>= 1) lf += __shfl_xor_sync(0xffffffffu, lf, k);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int row = grp + 32 * jj;
+          const int key = t * kRows + row;
+          const bool use = whole || key <= P;
+          const uint8_t* src = (!whole && key == P) ? reinterpret_cast<const uint8_t*>(sq + D) : kt + row * (2 * D);
+          if (use) kr[jj].load(src, l8);
+          float a0 = 0.0f, a1 = 0.0f;
+          if (use) {
 #pragma unroll
-    for (int d = 0; d < DH; ++d) red[(half * DH + d) * 128 + row] = o[d] * f;
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (lane == 0) mred[8 + warp - 1] = lf;
-    if (c < D) {
-      float acc = 0.0f;
-      for (int k = 0; k < 128; ++k) acc += red[c * 128 + (k + c) % 128];
-      part[c] = acc;
-    }
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (c == 0) {
-      float L = 0.0f;
-      for (int w = 0; w < 8; ++w) L += mred[8 + w];
-      part[D] = M;
-      part[D + 1] = L;
+            for (int v = 0; v < NV; ++v) {
+              const float x = kr[jj].at(v);
+              float coef;
+              if constexpr (SMALL_R && H2 > 0) {
+                coef = v < 8 ? fmaf(cb[v], sr[jj][v], ca[v] * cr[jj][v]) : zr[v];
+              } else if constexpr (SMALL_R) {
+                coef = zr[v];
+              } else {
+                const int d = lane_dim<D>(l8, v);
+                coef = zr[v];
+                if (d < p.r) {
+                  const int i = d < h2 ? d : d - h2;
+                  const float2 c = p.cs[static_cast<long long>(key) * h2 + i];
+                  coef = d < h2 ? zr[v] * c.x + zi[v] * c.y : zi[v] * c.x - zr[v] * c.y;
+                }
+              }
+              if (v & 1)
+                a1 = fmaf(coef, x, a1);
+              else
+                a0 = fmaf(coef, x, a0);
+            }
+          }
+          sc[jj] = a0 + a1;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], 1);
+          sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], 2);
+          sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], 4);
+          if (!whole && t * kRows + grp + 32 * jj > P) sc[jj] = -INFINITY;
+        }
+        // online softmax of the group's rows (log2 units), lazy rescale beyond 2^8
+        const float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        if (mx > m + 8.0f) {
+          const float f = ex2_approx(m - mx);
+          l *= f;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) o[v] *= f;
+          m = mx;
+        }
+        float pw[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) pw[jj] = sc[jj] == -INFINITY ? 0.0f : ex2_approx(sc[jj] - m);
+        l += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int row = grp + 32 * jj;
+          const int key = t * kRows + row;
+          if (whole || key <= P) {
+            const bool is_new = !whole && key == P;
+            const uint8_t* src = is_new ? reinterpret_cast<const uint8_t*>(sq + 2 * D) : vt + row * (2 * D);
+            LaneRow<D> vr;
+            vr.load(src, l8);
+#pragma unroll
+            for (int v = 0; v < NV; ++v) o[v] = fmaf(pw[jj], vr.at(v), o[v]);
+            if (is_new) {  // append the new token's raw key and value to the cache
+              const long long crow = (head * p.Smax + P) * D;
+              uint8_t* kd = reinterpret_cast<uint8_t*>(p.k_cache + crow);
+              uint8_t* vd = reinterpret_cast<uint8_t*>(p.v_cache + crow);
+              const uint8_t* ks = reinterpret_cast<const uint8_t*>(sq + D);
+              *reinterpret_cast<uint4*>(kd + 16 * l8) = *reinterpret_cast<const uint4*>(ks + 16 * l8);
+              *reinterpret_cast<uint4*>(vd + 16 * l8) = *reinterpret_cast<const uint4*>(src + 16 * l8);
+              if constexpr (D == 128) {
+                *reinterpret_cast<uint4*>(kd + 128 + 16 * l8) = *reinterpret_cast<const uint4*>(ks + 128 + 16 * l8);
+                *reinterpret_cast<uint4*>(vd + 128 + 16 * l8) = *reinterpret_cast<const uint4*>(src + 128 + 16 * l8);
+              }
+              if constexpr (D == 96) {
+                *reinterpret_cast<uint2*>(kd + 128 + 8 * l8) = *reinterpret_cast<const uint2*>(ks + 128 + 8 * l8);
+                *reinterpret_cast<uint2*>(vd + 128 + 8 * l8) = *reinterpret_cast<const uint2*>(src + 128 + 8 * l8);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(s));  // this warp is done with stage s
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty(slot));  // and with the item slot
+
+      // ---- merge the 32 row groups: the warp's 4 groups by shuffles, then the 8 warps
+#pragma unroll
+      for (int x = 8; x <= 16; x <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, x), lo2 = __shfl_xor_sync(0xffffffffu, l, x);
+        const float M = fmaxf(m, mo);
+        const float fs = m == -INFINITY ? 0.0f : ex2_approx(m - M);
+        const float fo = mo == -INFINITY ? 0.0f : ex2_approx(mo - M);
+        l = l * fs + lo2 * fo;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) o[v] = o[v] * fs + __shfl_xor_sync(0xffffffffu, o[v], x) * fo;
+        m = M;
+      }
+      float* rb = red + ((k & 1) * 8 + cw) * (D + 2);
+      if (lane < 8) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) rb[lane_dim<D>(l8, v)] = o[v];
+      }
+      if (lane == 0) {
+        rb[D] = m;
+        rb[D + 1] = l;
+      }
+      const bool stop = consumers_sync_or(!ok || *abort_flag != 0);
+      const int c = tid - 32;
+      if (c < D) {
+        const float* r0 = red + (k & 1) * 8 * (D + 2);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) M = fmaxf(M, r0[w * (D + 2) + D]);
+        float acc = 0.0f, L = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const float mw = r0[w * (D + 2) + D];
+          const float f = mw == -INFINITY ? 0.0f : ex2_approx(mw - M);
+          acc = fmaf(r0[w * (D + 2) + c], f, acc);
+          L = fmaf(r0[w * (D + 2) + D + 1], f, L);
+        }
+        const long long j = cta - dec_cta_of(head * Th, N, G);  // this run's slot among the head's
+        if (j >= 0 && j < p.runs_per_head) {
+          float* pp = p.part + (head * p.runs_per_head + j) * (D + 2);
+          pp[c] = acc;
+          if (c == 0) {
+            pp[D] = M;
+            pp[D + 1] = L;
+          }
+        } else if (c == 0) {
+          record_error(kErrBadInput, 1);
+        }
+      }
+      if (stop) break;
     }
   }
   __syncthreads();
 }
 
-// Merge the splits of head (b, h): M = max m_s, L = sum l_s 2^(m_s - M),
-// out = sum o_s 2^(m_s - M) / L, lse = ln 2 * (M + log2 L).
+// Merge the partial states of head (b, h): M = max m_s, L = sum l_s 2^(m_s - M),
+// out = sum o_s 2^(m_s - M) / L, lse = ln 2 * (M + log2 L).  A head with no valid
+// position (reported through the device error word) gets out = 0, lse = -inf.
 template <int D>
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodeParams p, int G) {
   const int h = blockIdx.x, b = blockIdx.y;
-  const float* part = p.part + (static_cast<int64_t>(b) * p.H + h) * p.splits * (D + 2);
+  const long long head = static_cast<long long>(b) * p.H + h;
+  const long long N = p.total_tiles;
+  const long long first = head * p.tiles_per_head;
+  const int runs = static_cast<int>(dec_cta_of(first + p.tiles_per_head - 1, N, G) - dec_cta_of(first, N, G)) + 1;
+  const int nr = min(runs, p.runs_per_head);
+  const float* part = p.part + head * p.runs_per_head * (D + 2);
   float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, part[s * (D + 2) + D]);
+  for (int s = 0; s < nr; ++s) M = fmaxf(M, part[s * (D + 2) + D]);
   float L = 0.0f;
-  for (int s = 0; s < p.splits; ++s) {
+  for (int s = 0; s < nr; ++s) {
     const float ms = part[s * (D + 2) + D];
     if (ms != -INFINITY) L += part[s * (D + 2) + D + 1] * ex2_approx(ms - M);
   }
-  const float inv_l = 1.0f / L;
+  const float inv_l = L > 0.0f ? 1.0f / L : 0.0f;
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     float acc = 0.0f;
-    for (int s = 0; s < p.splits; ++s) {
+    for (int s = 0; s < nr; ++s) {
       const float ms = part[s * (D + 2) + D];
       if (ms != -INFINITY) acc += part[s * (D + 2) + d] * ex2_approx(ms - M);
     }
-    p.out[(static_cast<int64_t>(b) * p.H + h) * D + d] = f32_to_bf16_bits(acc * inv_l);
+    p.out[head * D + d] = f32_to_bf16_bits(acc * inv_l);
   }
-  if (threadIdx.x == 0) p.lse[static_cast<int64_t>(b) * p.H + h] = (M + log2f(L)) * 0.69314718055994530942f;
+  if (threadIdx.x == 0) p.lse[head] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace neox

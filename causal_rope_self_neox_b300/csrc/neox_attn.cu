@@ -267,28 +267,28 @@ int validate_decode(const void* qkv_new, const void* k_cache, const void* v_cach
 }
 
 template <int D, int H2>
-int launch_decode_h2(const neox::DecodeParams& p, cudaStream_t stream) {
+int launch_decode_h2(const neox::DecodeParams& p, int ctas, cudaStream_t stream) {
   const int smem = neox::dec_smem_bytes(D);
   cudaError_t e = cudaFuncSetAttribute(neox::attn_decode_kernel<D, H2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  neox::attn_decode_kernel<D, H2><<<dim3(p.splits, p.H, p.B), neox::kDecThreads, smem, stream>>>(p);
+  neox::attn_decode_kernel<D, H2><<<ctas, neox::kDecThreads, smem, stream>>>(p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  neox::attn_decode_combine_kernel<D><<<dim3(p.H, p.B), 128, 0, stream>>>(p);
+  neox::attn_decode_combine_kernel<D><<<dim3(p.H, p.B), 128, 0, stream>>>(p, ctas);
   e = cudaGetLastError();
   return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
 }
 
-// rotary_dim 0, 8, 16, 24, 32: pairing fixed at compile time; others: the general path
+// rotary_dim 0, 8, 16, 24, 32: tile x row factorisation of the angle; others: the general path
 template <int D>
-int launch_decode(const neox::DecodeParams& p, int r, cudaStream_t stream) {
+int launch_decode(const neox::DecodeParams& p, int r, int ctas, cudaStream_t stream) {
   switch (r) {
-    case 0: return launch_decode_h2<D, 0>(p, stream);
-    case 8: return launch_decode_h2<D, 4>(p, stream);
-    case 16: return launch_decode_h2<D, 8>(p, stream);
-    case 24: return launch_decode_h2<D, 12>(p, stream);
-    case 32: return launch_decode_h2<D, 16>(p, stream);
-    default: return launch_decode_h2<D, -1>(p, stream);
+    case 0: return launch_decode_h2<D, 0>(p, ctas, stream);
+    case 8: return launch_decode_h2<D, 4>(p, ctas, stream);
+    case 16: return launch_decode_h2<D, 8>(p, ctas, stream);
+    case 24: return launch_decode_h2<D, 12>(p, ctas, stream);
+    case 32: return launch_decode_h2<D, 16>(p, ctas, stream);
+    default: return launch_decode_h2<D, -1>(p, ctas, stream);
   }
 }
 
@@ -382,15 +382,17 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
       rc = get_table(device, std::max(Smax, neox::kRows), rotary_dim, rotary_base, stream, &cs);
       if (rc != NEOX_OK) return rc;
     }
-    // key-range splits: about four CTAs per SM in total (one runs at a time); each CTA
-    // costs a start-up and a reduction, so a head is split only when there are few heads
+    // one CTA per SM, each with an equal contiguous range of the B*H*ceil(Smax/128) key
+    // tiles; a head's tiles fall into the ranges of at most runs_per_head CTAs (every range
+    // but the first and last inside the head covers at least N / G of its tiles)
     const int tiles = (Smax + neox::kRows - 1) / neox::kRows;
-    const int64_t heads = static_cast<int64_t>(B) * H;
-    int splits = static_cast<int>(std::min<int64_t>(tiles, std::max<int64_t>(1, (4 * dev.num_sms + heads - 1) / heads)));
-    const int tps = (tiles + splits - 1) / splits;
-    splits = (tiles + tps - 1) / tps;
+    const long long heads = static_cast<long long>(B) * H;
+    const long long N = heads * tiles;
+    const int ctas = static_cast<int>(std::min<long long>(dev.num_sms, N));
+    const long long q = N / ctas;
+    const int runs = tiles >= 2 ? static_cast<int>(std::min<long long>(tiles, (tiles - 2) / q + 2)) : 1;
     float* part = nullptr;
-    rc = get_scratch(device, static_cast<size_t>(heads) * splits * (D + 2) * sizeof(float), &part);
+    rc = get_scratch(device, static_cast<size_t>(heads) * runs * (D + 2) * sizeof(float), &part);
     if (rc != NEOX_OK) return rc;
     neox::DecodeParams p{};
     p.qkv_new = static_cast<const uint16_t*>(qkv_new);
@@ -405,14 +407,15 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
     p.H = H;
     p.Smax = Smax;
     p.r = rotary_dim;
-    p.splits = splits;
-    p.tiles_per_split = tps;
+    p.tiles_per_head = tiles;
+    p.runs_per_head = runs;
+    p.total_tiles = N;
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
     switch (D) {
-      case 64: return launch_decode<64>(p, rotary_dim, stream);
-      case 96: return launch_decode<96>(p, rotary_dim, stream);
-      default: return launch_decode<128>(p, rotary_dim, stream);
+      case 64: return launch_decode<64>(p, rotary_dim, ctas, stream);
+      case 96: return launch_decode<96>(p, rotary_dim, ctas, stream);
+      default: return launch_decode<128>(p, rotary_dim, ctas, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
