@@ -59,10 +59,14 @@ constexpr int kDecRingBytes = 192 * 1024;
 // ring stages of K + V tiles in 192 KB: 6 (D = 64), 4 (D = 96), 3 (D = 128)
 __host__ __device__ constexpr int dec_stages(int D) { return kDecRingBytes / (2 * tile_bytes(D)); }
 __host__ __device__ constexpr int dec_slot_bytes(int D) { return 3 * D * 2 + 16 * 8; }  // q|k|v, query angle
+// row factors of rows 0..127: per row 8 entries of 2 pairs (cos 2q, cos 2q+1, sin 2q,
+// sin 2q+1) and the identity (1, 1, 0, 0)
+constexpr int kDecRowTabBytes = kRows * 9 * 16;
 // smem: ring, 2 item slots, per stage the tile factor (16 float2 + the identity), the
-// cross-warp merge buffer [2][8][D + 2], barriers, abort flag and the slots' positions
+// cross-warp merge buffer [2][8][D + 2], the row factors, barriers, abort flag and the
+// slots' positions
 __host__ __device__ constexpr int dec_smem_bytes(int D) {
-  return kDecRingBytes + 2 * dec_slot_bytes(D) + dec_stages(D) * 18 * 8 + 2 * 8 * (D + 2) * 4 +
+  return kDecRingBytes + 2 * dec_slot_bytes(D) + dec_stages(D) * 18 * 8 + 2 * 8 * (D + 2) * 4 + kDecRowTabBytes +
          (2 * dec_stages(D) + 4) * 8 + 16 + 512;
 }
 
@@ -74,6 +78,15 @@ __host__ __device__ __forceinline__ long long dec_cta_of(long long x, long long 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float word_dim(uint32_t w, int odd) { return odd ? bf16hi(w) : bf16lo(w); }
+// two bf16 (lo, hi) as an fp32 pair, and fp32 pair helpers
+__device__ __forceinline__ uint64_t bf16x2_f32x2(uint32_t w) { return f32x2_pack(bf16lo(w), bf16hi(w)); }
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float f2lo(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x)); }
+__device__ __forceinline__ float f2hi(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x >> 32)); }
 
 // The D/8 dims lane l8 of a row group owns: v < 8 -> 8 l8 + v (chunk l8); v >= 8 ->
 // 64 + 8 l8 + (v - 8) (chunk l8 + 8, D = 128) or 64 + 4 l8 + (v - 8) (piece l8, D = 96).
@@ -104,6 +117,12 @@ struct LaneRow {
       return word_dim(q == 0 ? c1.x : q == 1 ? c1.y : q == 2 ? c1.z : c1.w, v & 1);
     }
     return word_dim(((v - 8) >> 1) == 0 ? pc.x : pc.y, v & 1);
+  }
+  // dims (2u, 2u + 1) of the lane as an fp32 pair
+  __device__ __forceinline__ uint64_t pair(int u) const {
+    if (u < 4) return bf16x2_f32x2(u == 0 ? c0.x : u == 1 ? c0.y : u == 2 ? c0.z : c0.w);
+    if constexpr (D == 128) return bf16x2_f32x2(u == 4 ? c1.x : u == 5 ? c1.y : u == 6 ? c1.z : c1.w);
+    return bf16x2_f32x2(u == 4 ? pc.x : pc.y);
   }
 };
 
@@ -136,7 +155,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   uint8_t* slots = smem + kDecRingBytes;                                  // [2][SLOT]
   float2* tf = reinterpret_cast<float2*>(slots + 2 * SLOT);              // [S][18]
   float* red = reinterpret_cast<float*>(tf + S * 18);                    // [2][8][D + 2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 2 * 8 * (D + 2));   // full, empty, qfull, qempty
+  float4* rtab = reinterpret_cast<float4*>(red + 2 * 8 * (D + 2));       // [128][H2/2 + 1]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(rtab) + kDecRowTabBytes);
   int* misc = reinterpret_cast<int*>(bars + 2 * S + 4);                  // abort flag, slot positions
   volatile int* abort_flag = misc;
   int* slot_pos = misc + 1;
@@ -243,17 +263,32 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     auto pair0 = [&](int v) { return rot_lane ? (8 * l8 + v < h2 ? 8 * l8 + v : 8 * l8 + v - h2) : 16; };
     auto is_a0 = [&](int v) { return !rot_lane || 8 * l8 + v < h2; };  // first half of its pair
     // row factors e^{j row w}: (cos, sin)(row w_pair) for rows grp + 32 jj
-    float cr[4][8], sr[4][8];
+    // row factors e^{j row w} of rows 0..127 into shared memory; lane entry u of a row
+    // covers chunk-0 dims (2u, 2u + 1): pairs 2q, 2q + 1 with q = qo[u] (dims 2u, 2u + 1
+    // of a rotated lane belong to consecutive pairs since r/2 is even), the identity on
+    // unrotated lanes
+    constexpr int RQ = (SMALL_R && H2 > 0 ? H2 / 2 : 0) + 1;  // entries per row
+    int qo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) qo[u] = rot_lane ? pair0(2 * u) / 2 : RQ - 1;
     if constexpr (SMALL_R && H2 > 0) {
-#pragma unroll
-      for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float2 f = rot_lane ? p.cs[(grp + 32 * jj) * H2 + pair0(v)] : make_float2(1.0f, 0.0f);
-          cr[jj][v] = f.x;
-          sr[jj][v] = f.y;
+      for (int e = tid - 32; e < kRows * RQ; e += 256) {
+        const int row = e / RQ, q = e - row * RQ;
+        float4 f = make_float4(1.0f, 1.0f, 0.0f, 0.0f);
+        if (q < RQ - 1) {
+          const float2 a = p.cs[row * H2 + 2 * q], b = p.cs[row * H2 + 2 * q + 1];
+          f = make_float4(a.x, b.x, a.y, b.y);
         }
+        rtab[e] = f;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
     }
+    // (cos, sin) of chunk-0 dims (2u, 2u + 1) of row `row`, packed over the two dims
+    auto row_factor = [&](int row, int u, uint64_t& c2, uint64_t& s2) {
+      const float4 f = rtab[row * RQ + qo[u]];
+      c2 = f32x2_pack(f.x, f.y);
+      s2 = f32x2_pack(f.z, f.w);
+    };
     uint32_t n = 0;
     int k = 0;
     for (long long g = lo; g < hi; ++k) {
@@ -288,9 +323,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
       }
       float m = -INFINITY, l = 0.0f;
-      float o[NV];
+      uint64_t o2[NV / 2];  // o over dims (2u, 2u + 1)
 #pragma unroll
-      for (int v = 0; v < NV; ++v) o[v] = 0.0f;
+      for (int u = 0; u < NV / 2; ++u) o2[u] = 0;
 
       for (int t = tb; ok && t < t1; ++t, ++n) {
         const int s = static_cast<int>(n % S);
@@ -301,8 +336,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         // chunk-0 coefficients of this tile: w = z e^{-j 128 t w}; dim i of a pair takes
         // Re(w e^{-j row w}) = wr c + wi s, dim i + h2 takes Im(...) = wi c - wr s
-        float ca[8], cb[8];
+        uint64_t ca2[4], cb2[4];
         if constexpr (SMALL_R && H2 > 0) {
+          float ca[8], cb[8];
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             const float2 f = tf[s * 18 + pair0(v)];
@@ -310,10 +346,65 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             ca[v] = is_a0(v) ? wr : wi;
             cb[v] = is_a0(v) ? wi : -wr;
           }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            ca2[u] = f32x2_pack(ca[2 * u], ca[2 * u + 1]);
+            cb2[u] = f32x2_pack(cb[2 * u], cb[2 * u + 1]);
+          }
         }
         const uint8_t* kt = smem + (2 * s) * TB;
         const uint8_t* vt = kt + TB;
         const bool whole = t * kRows + kRows - 1 < P;  // every row valid, none is the new token
+        if (SMALL_R && whole) {
+          // ---- a full tile of cached keys: all loads first, then packed fp32 math
+          LaneRow<D> kr[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) kr[jj].load(kt + (grp + 32 * jj) * (2 * D), l8);
+          float sc[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint64_t acc = 0;
+#pragma unroll
+            for (int u = 0; u < NV / 2; ++u) {
+              uint64_t coef;
+              if (H2 > 0 && u < 4) {
+                uint64_t c2, s2;
+                row_factor(grp + 32 * jj, u, c2, s2);
+                coef = ffma2(cb2[u], s2, fmul2(ca2[u], c2));
+              } else
+                coef = f32x2_pack(zr[2 * u], zr[2 * u + 1]);
+              acc = ffma2(coef, kr[jj].pair(u), acc);
+            }
+            sc[jj] = f2lo(acc) + f2hi(acc);
+          }
+          LaneRow<D> vr[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) vr[jj].load(vt + (grp + 32 * jj) * (2 * D), l8);
+#pragma unroll
+          for (int x = 1; x <= 4; x <<= 1)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], x);
+          const float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+          if (mx > m + 8.0f) {
+            const float f = ex2_approx(m - mx);
+            l *= f;
+            const uint64_t f2 = f32x2_pack(f, f);
+#pragma unroll
+            for (int u = 0; u < NV / 2; ++u) o2[u] = fmul2(o2[u], f2);
+            m = mx;
+          }
+          float pw[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) pw[jj] = ex2_approx(sc[jj] - m);
+          l += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint64_t pp = f32x2_pack(pw[jj], pw[jj]);
+#pragma unroll
+            for (int u = 0; u < NV / 2; ++u) o2[u] = ffma2(vr[jj].pair(u), pp, o2[u]);
+          }
+        } else {
+        // ---- general tile: masked rows past P, the new token's row, any rotary_dim
         float sc[4];
         LaneRow<D> kr[4];
 #pragma unroll
@@ -330,7 +421,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               const float x = kr[jj].at(v);
               float coef;
               if constexpr (SMALL_R && H2 > 0) {
-                coef = v < 8 ? fmaf(cb[v], sr[jj][v], ca[v] * cr[jj][v]) : zr[v];
+                if (v < 8) {
+                  uint64_t c2, s2;
+                  row_factor(row, v >> 1, c2, s2);
+                  const float crv = (v & 1) ? f2hi(c2) : f2lo(c2), srv = (v & 1) ? f2hi(s2) : f2lo(s2);
+                  const float cav = (v & 1) ? f2hi(ca2[v >> 1]) : f2lo(ca2[v >> 1]);
+                  const float cbv = (v & 1) ? f2hi(cb2[v >> 1]) : f2lo(cb2[v >> 1]);
+                  coef = fmaf(cbv, srv, cav * crv);
+                } else {
+                  coef = zr[v];
+                }
               } else if constexpr (SMALL_R) {
                 coef = zr[v];
               } else {
@@ -362,8 +462,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (mx > m + 8.0f) {
           const float f = ex2_approx(m - mx);
           l *= f;
+          const uint64_t f2 = f32x2_pack(f, f);
 #pragma unroll
-          for (int v = 0; v < NV; ++v) o[v] *= f;
+          for (int u = 0; u < NV / 2; ++u) o2[u] = fmul2(o2[u], f2);
           m = mx;
         }
         float pw[4];
@@ -379,8 +480,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const uint8_t* src = is_new ? reinterpret_cast<const uint8_t*>(sq + 2 * D) : vt + row * (2 * D);
             LaneRow<D> vr;
             vr.load(src, l8);
+            const uint64_t pp = f32x2_pack(pw[jj], pw[jj]);
 #pragma unroll
-            for (int v = 0; v < NV; ++v) o[v] = fmaf(pw[jj], vr.at(v), o[v]);
+            for (int u = 0; u < NV / 2; ++u) o2[u] = ffma2(vr.pair(u), pp, o2[u]);
             if (is_new) {  // append the new token's raw key and value to the cache
               const long long crow = (head * p.Smax + P) * D;
               uint8_t* kd = reinterpret_cast<uint8_t*>(p.k_cache + crow);
@@ -399,6 +501,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
           }
         }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty(s));  // this warp is done with stage s
       }
@@ -414,13 +517,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const float fo = mo == -INFINITY ? 0.0f : ex2_approx(mo - M);
         l = l * fs + lo2 * fo;
 #pragma unroll
-        for (int v = 0; v < NV; ++v) o[v] = o[v] * fs + __shfl_xor_sync(0xffffffffu, o[v], x) * fo;
+        for (int u = 0; u < NV / 2; ++u) {
+          const float a = f2lo(o2[u]), b = f2hi(o2[u]);
+          o2[u] = f32x2_pack(a * fs + __shfl_xor_sync(0xffffffffu, a, x) * fo,
+                             b * fs + __shfl_xor_sync(0xffffffffu, b, x) * fo);
+        }
         m = M;
       }
       float* rb = red + ((k & 1) * 8 + cw) * (D + 2);
       if (lane < 8) {
 #pragma unroll
-        for (int v = 0; v < NV; ++v) rb[lane_dim<D>(l8, v)] = o[v];
+        for (int v = 0; v < NV; ++v) rb[lane_dim<D>(l8, v)] = (v & 1) ? f2hi(o2[v >> 1]) : f2lo(o2[v >> 1]);
       }
       if (lane == 0) {
         rb[D] = m;
