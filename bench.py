@@ -64,12 +64,13 @@ def load_peaks():
 
 
 FWD_KERNEL_SOURCES = ("attn_ws.cuh", "attn_common.cuh", "ptx.cuh", "rotary.cuh", "tile_layout.cuh")
+DEC_KERNEL_SOURCES = ("decode.cuh", "attn_common.cuh", "ptx.cuh", "tile_layout.cuh", "neox_attn.cu")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources the prefill kernel is compiled from (not the decode path)."""
+def kernel_source_hash(sources=FWD_KERNEL_SOURCES) -> str:
+    """Hash of the sources a kernel is compiled and launched from (by default the prefill kernel's)."""
     h = hashlib.sha256()
-    files = [os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", n) for n in FWD_KERNEL_SOURCES]
+    files = [os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", n) for n in sources]
     for f in files:
         with open(f, "rb") as fh:
             h.update(os.path.basename(f).encode())
@@ -77,11 +78,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, prefix: str = "attn_fwd_ws", sources=FWD_KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu summary of this workload
-    (profiles/attn_fwd_ws_<workload>.txt, `key: value` lines), if it was taken on the
+    (profiles/<prefix>_<workload>.txt, `key: value` lines), if it was taken on the
     current kernel sources; otherwise None."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_ws_{workload}.txt")
+    path = os.path.join(ROOT, "profiles", f"{prefix}_{workload}.txt")
     prof = {}
     try:
         with open(path) as f:
@@ -91,7 +92,7 @@ def profiled_traffic(workload: str):
                     prof[k.strip()] = v.strip()
     except OSError:
         return None, "no ncu summary"
-    if prof.get("source_hash") != kernel_source_hash():
+    if prof.get("source_hash") != kernel_source_hash(sources):
         return None, "kernel changed since the ncu capture"
     try:
         return float(prof["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
@@ -471,6 +472,7 @@ def run_decode(args, w):
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     na.check_device_error()
     _, _, hbm, src = load_peaks()
+    traffic, tsrc = profiled_traffic(w.name, "attn_decode", DEC_KERNEL_SOURCES)
     line = {
         "metric": DECODE_METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -478,8 +480,8 @@ def run_decode(args, w):
         "tokens_per_s": w.B / (ms_per_step / 1e3),
         "config": {**w.describe(), "l2": "flushed before every step (256 MB write, outside the event interval)"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                     "traffic": None, "peak_kind": f"{src} HBM copy bandwidth",
-                     "kernel": f"attn_decode_kernel<D={w.D}> + combine",
+                     "traffic": traffic, "traffic_source": tsrc, "peak_kind": f"{src} HBM copy bandwidth",
+                     "kernel": f"attn_decode_kernel<D={w.D}> + combine (both in the timed step)",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
         "e2e": {"value": alg_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
