@@ -12,7 +12,7 @@
 //   attn_decode_kernel: persistent, one CTA per SM.  The B*H*ceil(Smax/128) key tiles of
 //     all heads, taken head after head, are cut into one contiguous range per CTA (equal
 //     to within one tile, whatever B, H and Smax are); the run of a range inside one head
-//     is a work item whose partial softmax state (m, l, o[D]) goes to a scratch slot.
+//     is a work item.
 //     Warp 0 streams the items' K and V tiles (one bulk copy per operand: a head's cache
 //     rows are contiguous) through a shared-memory ring that runs on across items, and
 //     each item's new-token row (q, k, v) and query angle into one of two item slots.
@@ -22,7 +22,9 @@
 //     lanes reading one row touch 8 distinct bank groups.  Partial dot products meet in
 //     three shuffles; each group keeps its own online softmax; at the end of an item the
 //     groups merge by shuffles inside a warp and through shared memory across warps.
-//   attn_decode_combine_kernel: merges the partial states of a head into out and lse.
+//   A head inside one CTA's range is written out by that CTA; a head spanning several
+//   ranges leaves one partial state per range, and the last of its CTAs to finish (a
+//   per-head arrival counter, reset to zero by that CTA) merges them into out and lse.
 // Rotation, with the cache keys unrotated: for pair (i, i + r/2) and key angle phi,
 //   q'_i k'_i + q'_{i+r/2} k'_{i+r/2} = k_i Re(z e^{-j phi}) + k_{i+r/2} Im(z e^{-j phi}),
 // z = q'_i + j q'_{i+r/2}, so the query is turned instead of the key.  For r = 8..32 all
@@ -44,6 +46,7 @@ struct DecodeParams {
   const int* pos;           // int32 [B]
   const float2* cs;         // cos/sin table [max(Smax, 128) rows][r/2]
   float* part;              // fp32 [B*H][runs_per_head][D + 2]: o[D], m, l  (m in log2 units)
+  int* counters;            // int32 [B*H], zero between calls: runs of a head merged so far
   uint16_t* out;            // bf16 [B, H, D]
   float* lse;               // fp32 [B, H]
   int B, H, Smax, r;
@@ -126,6 +129,16 @@ struct LaneRow {
   }
 };
 
+// Final output of head `head`, dim c, from a merged state (m in log2 units):
+// out = o / l (bf16), lse = ln 2 * (m + log2 l); a head with no valid position (l = 0,
+// reported through the device error word) gets out = 0, lse = -inf.
+template <int D>
+__device__ __forceinline__ void dec_write_out(const DecodeParams& p, long long head, int c, float o, float m,
+                                              float l) {
+  p.out[head * D + c] = f32_to_bf16_bits(l > 0.0f ? o * (1.0f / l) : 0.0f);
+  if (c == 0) p.lse[head] = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+}
+
 // Named barrier over the 256 consumer threads that also ORs a flag across them.
 __device__ __forceinline__ bool consumers_sync_or(bool flag) {
   uint32_t res;
@@ -160,6 +173,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   int* misc = reinterpret_cast<int*>(bars + 2 * S + 4);                  // abort flag, slot positions
   volatile int* abort_flag = misc;
   int* slot_pos = misc + 1;
+  volatile int* last_flag = misc + 3;
   auto full = [&](int s) { return smem_u32(&bars[s]); };
   auto empty = [&](int s) { return smem_u32(&bars[S + s]); };
   auto qfull = [&](int i) { return smem_u32(&bars[2 * S + i]); };
@@ -534,13 +548,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         rb[D + 1] = l;
       }
       const bool stop = consumers_sync_or(!ok || *abort_flag != 0);
+      if (stop) break;
       const int c = tid - 32;
+      float M = -INFINITY, acc = 0.0f, L = 0.0f;
       if (c < D) {
         const float* r0 = red + (k & 1) * 8 * (D + 2);
-        float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < 8; ++w) M = fmaxf(M, r0[w * (D + 2) + D]);
-        float acc = 0.0f, L = 0.0f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) {
           const float mw = r0[w * (D + 2) + D];
@@ -548,53 +562,52 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           acc = fmaf(r0[w * (D + 2) + c], f, acc);
           L = fmaf(r0[w * (D + 2) + D + 1], f, L);
         }
-        const long long j = cta - dec_cta_of(head * Th, N, G);  // this run's slot among the head's
-        if (j >= 0 && j < p.runs_per_head) {
-          float* pp = p.part + (head * p.runs_per_head + j) * (D + 2);
+      }
+      // the CTAs whose tile ranges hold part of this head (the same for every thread)
+      const long long cfirst = dec_cta_of(head * Th, N, G);
+      const int runs = static_cast<int>(dec_cta_of(head * Th + Th - 1, N, G) - cfirst) + 1;
+      if (runs == 1) {  // the whole head is this item
+        if (c < D) dec_write_out<D>(p, head, c, acc, M, L);
+      } else if (runs <= p.runs_per_head) {
+        // partial state to this run's slot; the last of the head's CTAs to arrive merges
+        float* hp = p.part + head * p.runs_per_head * (D + 2);
+        if (c < D) {
+          float* pp = hp + (cta - cfirst) * (D + 2);
           pp[c] = acc;
           if (c == 0) {
             pp[D] = M;
             pp[D + 1] = L;
           }
-        } else if (c == 0) {
-          record_error(kErrBadInput, 1);
+          __threadfence();
         }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (c == 0) {
+          const bool last = atomicAdd(p.counters + head, 1) == runs - 1;
+          if (last) p.counters[head] = 0;  // every run has arrived: ready for the next call
+          *last_flag = last ? 1 : 0;
+        }
+        asm volatile("bar.sync 1, 256;" ::: "memory");
+        if (*last_flag && c < D) {
+          __threadfence();
+          float Mh = -INFINITY;
+          for (int r = 0; r < runs; ++r) Mh = fmaxf(Mh, __ldcg(hp + r * (D + 2) + D));
+          float a = 0.0f, Lh = 0.0f;
+          for (int r = 0; r < runs; ++r) {
+            const float mr = __ldcg(hp + r * (D + 2) + D);
+            if (mr != -INFINITY) {
+              const float f = ex2_approx(mr - Mh);
+              a = fmaf(__ldcg(hp + r * (D + 2) + c), f, a);
+              Lh = fmaf(__ldcg(hp + r * (D + 2) + D + 1), f, Lh);
+            }
+          }
+          dec_write_out<D>(p, head, c, a, Mh, Lh);
+        }
+      } else if (c == 0) {
+        record_error(kErrBadInput, 1);
       }
-      if (stop) break;
     }
   }
   __syncthreads();
-}
-
-// Merge the partial states of head (b, h): M = max m_s, L = sum l_s 2^(m_s - M),
-// out = sum o_s 2^(m_s - M) / L, lse = ln 2 * (M + log2 L).  A head with no valid
-// position (reported through the device error word) gets out = 0, lse = -inf.
-template <int D>
-__global__ void __launch_bounds__(128) attn_decode_combine_kernel(const DecodeParams p, int G) {
-  const int h = blockIdx.x, b = blockIdx.y;
-  const long long head = static_cast<long long>(b) * p.H + h;
-  const long long N = p.total_tiles;
-  const long long first = head * p.tiles_per_head;
-  const int runs = static_cast<int>(dec_cta_of(first + p.tiles_per_head - 1, N, G) - dec_cta_of(first, N, G)) + 1;
-  const int nr = min(runs, p.runs_per_head);
-  const float* part = p.part + head * p.runs_per_head * (D + 2);
-  float M = -INFINITY;
-  for (int s = 0; s < nr; ++s) M = fmaxf(M, part[s * (D + 2) + D]);
-  float L = 0.0f;
-  for (int s = 0; s < nr; ++s) {
-    const float ms = part[s * (D + 2) + D];
-    if (ms != -INFINITY) L += part[s * (D + 2) + D + 1] * ex2_approx(ms - M);
-  }
-  const float inv_l = L > 0.0f ? 1.0f / L : 0.0f;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.0f;
-    for (int s = 0; s < nr; ++s) {
-      const float ms = part[s * (D + 2) + D];
-      if (ms != -INFINITY) acc += part[s * (D + 2) + d] * ex2_approx(ms - M);
-    }
-    p.out[head * D + d] = f32_to_bf16_bits(acc * inv_l);
-  }
-  if (threadIdx.x == 0) p.lse[head] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994530942f : -INFINITY;
 }
 
 }  // namespace neox

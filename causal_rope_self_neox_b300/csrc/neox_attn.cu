@@ -206,36 +206,63 @@ int launch_ws(Prepared& P, cudaStream_t stream) {
 }
 
 // ------------------------------------------------------------------- decode ----
-// Per-device fp32 scratch for the partial results of the decode key-range splits.
+// Per-device decode scratch: fp32 partial states of heads that span several CTAs, and one
+// int32 arrival counter per head (zeroed when allocated; every launch leaves them zero,
+// except one that gave up on a timed-out wait, after which the error report re-zeroes them).
 struct Scratch {
   int device;
   size_t bytes;
   float* ptr;
+  size_t counters;  // entries
+  int* cnt;
 };
 std::vector<Scratch> g_scratch;  // guarded by g_tab_mu
 
-int get_scratch(int device, size_t bytes, float** out) {
+int get_scratch(int device, size_t bytes, size_t heads, float** out, int** cnt) {
   std::lock_guard<std::mutex> lk(g_tab_mu);
   for (auto it = g_scratch.begin(); it != g_scratch.end(); ++it) {
     if (it->device == device) {
-      if (it->bytes >= bytes) {
+      if (it->bytes >= bytes && it->counters >= heads) {
         *out = it->ptr;
+        *cnt = it->cnt;
         return NEOX_OK;
       }
       cudaError_t e = cudaDeviceSynchronize();  // in-flight kernels may still use it
       if (e != cudaSuccess) return cuda_fail(e);
       cudaFree(it->ptr);
+      cudaFree(it->cnt);
+      bytes = std::max(bytes, it->bytes);
+      heads = std::max(heads, it->counters);
       g_scratch.erase(it);
       break;
     }
   }
   const size_t grown = std::max<size_t>(bytes, size_t(1) << 20);
+  const size_t ncnt = std::max<size_t>(heads, 4096);
   float* ptr = nullptr;
+  int* c = nullptr;
   cudaError_t e = cudaMalloc(&ptr, grown);
   if (e != cudaSuccess) return cuda_fail(e);
-  g_scratch.push_back(Scratch{device, grown, ptr});
+  e = cudaMalloc(&c, ncnt * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c, 0, ncnt * sizeof(int));
+  if (e != cudaSuccess) {
+    cudaFree(ptr);
+    if (c) cudaFree(c);
+    return cuda_fail(e);
+  }
+  g_scratch.push_back(Scratch{device, grown, ptr, ncnt, c});
   *out = ptr;
+  *cnt = c;
   return NEOX_OK;
+}
+
+// After a wait timed out, heads may have been left half-counted: zero every counter.
+void reset_decode_counters() {
+  std::lock_guard<std::mutex> lk(g_tab_mu);
+  for (auto& t : g_scratch) {
+    int cur = 0;
+    if (cudaGetDevice(&cur) == cudaSuccess && cur == t.device) cudaMemset(t.cnt, 0, t.counters * sizeof(int));
+  }
 }
 
 int validate_decode(const void* qkv_new, const void* k_cache, const void* v_cache, const int* pos, int B, int H,
@@ -273,8 +300,6 @@ int launch_decode_h2(const neox::DecodeParams& p, int ctas, cudaStream_t stream)
                                        smem);
   if (e != cudaSuccess) return cuda_fail(e);
   neox::attn_decode_kernel<D, H2><<<ctas, neox::kDecThreads, smem, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  neox::attn_decode_combine_kernel<D><<<dim3(p.H, p.B), 128, 0, stream>>>(p, ctas);
   e = cudaGetLastError();
   return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
 }
@@ -392,7 +417,9 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
     const long long q = N / ctas;
     const int runs = tiles >= 2 ? static_cast<int>(std::min<long long>(tiles, (tiles - 2) / q + 2)) : 1;
     float* part = nullptr;
-    rc = get_scratch(device, static_cast<size_t>(heads) * runs * (D + 2) * sizeof(float), &part);
+    int* counters = nullptr;
+    rc = get_scratch(device, static_cast<size_t>(heads) * runs * (D + 2) * sizeof(float), static_cast<size_t>(heads),
+                     &part, &counters);
     if (rc != NEOX_OK) return rc;
     neox::DecodeParams p{};
     p.qkv_new = static_cast<const uint16_t*>(qkv_new);
@@ -401,6 +428,7 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
     p.pos = pos;
     p.cs = cs;
     p.part = part;
+    p.counters = counters;
     p.out = static_cast<uint16_t*>(out);
     p.lse = lse;
     p.B = B;
@@ -430,6 +458,7 @@ int neox_attn_get_device_error(void) {
   const unsigned int zero = 0;
   e = cudaMemcpyToSymbol(neox::g_device_error, &zero, sizeof zero);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (v & neox::kErrTimeout) reset_decode_counters();
   return (v & neox::kErrTimeout) ? NEOX_ERR_DEVICE_TIMEOUT : NEOX_ERR_DEVICE_BAD_POSITION;
 }
 
@@ -470,6 +499,7 @@ void neox_attn_release(void) {
       cudaSetDevice(t.device);
       cudaDeviceSynchronize();
       cudaFree(t.ptr);
+      cudaFree(t.cnt);
     }
     cudaSetDevice(cur);
     g_scratch.clear();

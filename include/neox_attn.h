@@ -147,9 +147,13 @@ int neox_attn_fwd_noalloc(const void* qkv, int B, int S, int H, int D, int rotar
  *   stream       a cudaStream_t (NULL = legacy default stream).
  *
  * Ownership and errors as for neox_attn_fwd.  Besides the cos/sin table the library
- * owns a per-device fp32 scratch buffer for the partial results of the key-range
- * splits (grown on demand like the table; the call that grows it synchronizes the
- * device once; neox_attn_release() frees it).
+ * owns a per-device scratch: fp32 partial results of heads whose keys are split
+ * between several CTAs, and one int32 arrival counter per head that every call
+ * leaves at zero (grown on demand like the table; the call that grows it
+ * synchronizes the device once; neox_attn_release() frees it).  Calls share the
+ * scratch, so decode calls must not overlap on the GPU (different streams with no
+ * ordering between them).  After a NEOX_ERR_DEVICE_TIMEOUT report,
+ * neox_attn_get_device_error() re-zeroes the counters.
  */
 int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const int* pos, int B, int H, int Smax,
                      int D, int rotary_dim, float rotary_base, void* out, float* lse, void* stream);

@@ -90,3 +90,21 @@ def test_decode_bad_position_is_reported_and_the_context_survives():
     assert na.neox_attn_get_device_error() == na.NEOX_OK
     assert torch.equal(dk[1].cpu().view(torch.int16), kc[1].view(torch.int16))  # nothing written for b = 1
     check(new, kc, vc, [5, 63], 16, "after a bad position")
+
+
+def test_decode_repeated_calls_are_bit_identical():
+    # heads split between several CTAs merge through per-head arrival counters that each
+    # call must leave at zero: a second and third call give the same bits
+    import causal_rope_self_neox_b300 as na
+    B, H, Smax, D = 3, 5, 1200, 96
+    new, kc, vc = make_decode_inputs(B, H, Smax, D, seed=11)
+    dn, dk, dv = new.cuda(), kc.cuda(), vc.cuda()
+    dp = torch.tensor([1199, 640, 5], dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(3):
+        out, lse = na.attn_decode(dn, dk, dv, dp, 24)
+        outs.append((out.view(torch.int16).cpu(), lse.cpu()))
+    na.check_device_error()
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l.view(torch.int32), outs[0][1].view(torch.int32))
+    check(new, kc, vc, [1199, 640, 5], 24, "after repeated calls")
