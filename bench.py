@@ -7,7 +7,9 @@ A step is one pass of the whole op (rotary + QK^T + causal online softmax + PV +
 epilogue, one kernel launch) over the GPT-NeoX-20B-shaped workload (B=2, H=64,
 S=2048, D=96, rotary_dim=24) unless --workload says otherwise.  Inputs are seeded,
 synthetic and already resident in HBM when the timed region starts; L2 is flushed
-(a 256 MB write) before every step, outside the per-step CUDA-event interval.
+before every step, outside the per-step CUDA-event interval (a 256 MB write, then a
+256 MB read of another buffer, so that no dirty line of the flush is written back
+inside the step).
 Metric: causal FLOPs 2*B*H*S^2*D per step / kernel time, in TFLOP/s, and that figure
 as a fraction of the measured dense bf16 tensor peak.
 
@@ -43,6 +45,23 @@ from causal_rope_self_neox_b300.workloads import (DECODE_WORKLOADS, WORKLOADS, b
 
 METRIC = "causal RoPE attention fwd TFLOP/s and % of B300 bf16 tensor peak"
 L2_FLUSH_BYTES = 256 << 20
+L2_NOTE = ("flushed before every step, outside the event interval: a 256 MB write, then a 256 MB read of "
+           "another buffer, so L2 holds clean unrelated lines (no write-back of the flush inside the step)")
+
+
+class L2Flush:
+    """Evicts L2 between timed steps: writes one buffer larger than L2, then reads another,
+    so the step starts with neither its inputs nor dirty lines of the flush in L2."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.w.zero_()
+        self.torch.sum(self.r, dim=0, out=self.sink)
 FALLBACK_BF16_TFLOPS = 1800.0
 FALLBACK_HBM_GBS = 6400.0
 BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
@@ -272,7 +291,7 @@ def run_ours(args, w):
     qkv = qkv_cpu.to(dev)
     out = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
@@ -283,7 +302,7 @@ def run_ours(args, w):
             raise na.NeoxAttnError(rc, "neox_attn_fwd")
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     na.check_device_error()
     if not bool(torch.isfinite(lse).all()):
@@ -305,7 +324,7 @@ def run_ours(args, w):
         with ClockSampler(gpu_id) as cs:
             t0 = time.perf_counter()
             for i in range(args.steps):
-                flush.zero_()
+                flush()
                 starts[i].record(stream)
                 step()
                 ends[i].record(stream)
@@ -362,7 +381,7 @@ def run_ours(args, w):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, K x k_scale)",
-            "config": {**w.describe(), "l2": "flushed before every step (256 MB write, outside the event interval)",
+            "config": {**w.describe(), "l2": L2_NOTE,
                        "parallelism": f"replicas x{world} (each rank its own workload; no collective on the data path)"},
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s",
                          "frac": per_gpu / peak, "traffic": traffic,
@@ -410,7 +429,7 @@ def run_decode(args, w):
     pos = pos_cpu.to(dev)
     out = torch.empty((w.B, w.H, w.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
@@ -421,7 +440,7 @@ def run_decode(args, w):
             raise na.NeoxAttnError(rc, "neox_attn_decode")
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     na.check_device_error()
     props = torch.cuda.get_device_properties(dev)
@@ -437,7 +456,7 @@ def run_decode(args, w):
     with ClockSampler(gpu_id) as cs:
         t0 = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
+            flush()
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -478,7 +497,7 @@ def run_decode(args, w):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 caches and new tokens)",
         "tokens_per_s": w.B / (ms_per_step / 1e3),
-        "config": {**w.describe(), "l2": "flushed before every step (256 MB write, outside the event interval)"},
+        "config": {**w.describe(), "l2": L2_NOTE},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                      "traffic": traffic, "traffic_source": tsrc, "peak_kind": f"{src} HBM copy bandwidth",
                      "kernel": f"attn_decode_kernel<D={w.D}> (one launch per step)",
