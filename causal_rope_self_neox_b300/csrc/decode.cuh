@@ -16,9 +16,10 @@
 //     Warp 0 streams the items' K and V tiles (one bulk copy per operand: a head's cache
 //     rows are contiguous) through a shared-memory ring that runs on across items, and
 //     each item's new-token row (q, k, v) and query angle into one of two item slots.
-//     Warps 1-8 form 32 row groups of 8 lanes; group g takes rows g, g+32, g+64, g+96 of
-//     every tile, and lane l of a group owns D/8 dims of the row (16-byte chunk l, plus
-//     chunk l+8 for D = 128 or the 8-byte piece l of dims 64..95 for D = 96), so the 8
+//     The 8 consumer warps form NG = 32 row groups of 8 lanes; group g takes rows g,
+//     g + 32, g + 64, g + 96 of every tile, and
+//     lane l of a group owns D/8 dims of the row (16-byte chunk l, plus chunk l+8 for
+//     D = 128 or the 8-byte piece l of dims 64..95 for D = 96), so the 8
 //     lanes reading one row touch 8 distinct bank groups.  Partial dot products meet in
 //     three shuffles; each group keeps its own online softmax; at the end of an item the
 //     groups merge by shuffles inside a warp and through shared memory across warps.
@@ -30,7 +31,7 @@
 // z = q'_i + j q'_{i+r/2}, so the query is turned instead of the key.  For r = 8..32 all
 // rotated dims sit in chunk 0 of lanes 0..r/8-1, and e^{-j phi} of key 128 t + row splits
 // into a tile factor (applied to z once per tile) and a row factor (held in registers:
-// each lane sees the same 4 rows in every tile); the product of the two fp32 table entries
+// each lane sees the same rows in every tile); the product of the two fp32 table entries
 // is within ~3e-7 of the exact value, far below the 2^-9 of the bf16 inputs.  Other r
 // read each key's angle from the table.
 #pragma once
@@ -57,7 +58,12 @@ struct DecodeParams {
   uint64_t wait_limit_ns;
 };
 
-constexpr int kDecThreads = 288;  // warp 0: copies; warps 1-8: 32 row groups of 8 lanes
+// warp 0: copies; then CW consumer warps = 4 CW row groups of 8 lanes, each group 128/(4 CW)
+// rows of every tile.  CW = 8 for every D: 16 warps (2 rows per group) measured 16% slower
+// for D = 64 (a 544-thread CTA caps a thread at 96 registers, and the per-tile work of a
+// group is spread over fewer rows).
+__host__ __device__ constexpr int dec_consumer_warps(int) { return 8; }
+__host__ __device__ constexpr int dec_threads(int D) { return 32 + 32 * dec_consumer_warps(D); }
 constexpr int kDecRingBytes = 192 * 1024;
 // ring stages of K + V tiles in 192 KB: 6 (D = 64), 4 (D = 96), 3 (D = 128)
 __host__ __device__ constexpr int dec_stages(int D) { return kDecRingBytes / (2 * tile_bytes(D)); }
@@ -69,7 +75,8 @@ constexpr int kDecRowTabBytes = kRows * 9 * 16;
 // cross-warp merge buffer [2][8][D + 2], the row factors, barriers, abort flag and the
 // slots' positions
 __host__ __device__ constexpr int dec_smem_bytes(int D) {
-  return kDecRingBytes + 2 * dec_slot_bytes(D) + dec_stages(D) * 18 * 8 + 2 * 8 * (D + 2) * 4 + kDecRowTabBytes +
+  return kDecRingBytes + 2 * dec_slot_bytes(D) + dec_stages(D) * 18 * 8 + 2 * dec_consumer_warps(D) * (D + 2) * 4 +
+         kDecRowTabBytes +
          (2 * dec_stages(D) + 4) * 8 + 16 + 512;
 }
 
@@ -129,6 +136,17 @@ struct LaneRow {
   }
 };
 
+template <int N>
+__device__ __forceinline__ float dec_max(const float (&x)[N]) {
+  if constexpr (N == 2) return fmaxf(x[0], x[1]);
+  return fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+}
+template <int N>
+__device__ __forceinline__ float dec_sum(const float (&x)[N]) {
+  if constexpr (N == 2) return x[0] + x[1];
+  return (x[0] + x[1]) + (x[2] + x[3]);
+}
+
 // Final output of head `head`, dim c, from a merged state (m in log2 units):
 // out = o / l (bf16), lse = ln 2 * (m + log2 l); a head with no valid position (l = 0,
 // reported through the device error word) gets out = 0, lse = -inf.
@@ -139,16 +157,21 @@ __device__ __forceinline__ void dec_write_out(const DecodeParams& p, long long h
   if (c == 0) p.lse[head] = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
 }
 
-// Named barrier over the 256 consumer threads that also ORs a flag across them.
+// Named barrier 1 over the NT consumer threads, plain and OR-reducing a flag.
+template <int NT>
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+template <int NT>
 __device__ __forceinline__ bool consumers_sync_or(bool flag) {
   uint32_t res;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 q, %1, 0;\n\t"
-      "barrier.cta.red.or.pred p, 1, 256, q;\n\t"
+      "barrier.cta.red.or.pred p, 1, %2, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(res)
-      : "r"(static_cast<uint32_t>(flag))
+      : "r"(static_cast<uint32_t>(flag)), "n"(NT)
       : "memory");
   return res != 0;
 }
@@ -156,9 +179,13 @@ __device__ __forceinline__ bool consumers_sync_or(bool flag) {
 // H2 = rotary_dim / 2 when it is 0, 4, 8, 12 or 16 (tile x row factorisation of the
 // angle), or -1 for any other rotary_dim (one table read per key and rotated dim).
 template <int D, int H2>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(dec_threads(D), 1)
     attn_decode_kernel(const DecodeParams p) {
   constexpr bool SMALL_R = H2 >= 0;
+  constexpr int CW = dec_consumer_warps(D);  // consumer warps
+  constexpr int NCT = 32 * CW;               // consumer threads
+  constexpr int NG = 4 * CW;                 // row groups
+  constexpr int RPG = kRows / NG;            // rows of a tile per group
   constexpr int NV = D / 8;  // dims per lane
   constexpr int S = dec_stages(D);
   constexpr int TB = tile_bytes(D);
@@ -167,8 +194,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 511) & ~uintptr_t(511));
   uint8_t* slots = smem + kDecRingBytes;                                  // [2][SLOT]
   float2* tf = reinterpret_cast<float2*>(slots + 2 * SLOT);              // [S][18]
-  float* red = reinterpret_cast<float*>(tf + S * 18);                    // [2][8][D + 2]
-  float4* rtab = reinterpret_cast<float4*>(red + 2 * 8 * (D + 2));       // [128][H2/2 + 1]
+  float* red = reinterpret_cast<float*>(tf + S * 18);                    // [2][CW][D + 2]
+  float4* rtab = reinterpret_cast<float4*>(red + 2 * CW * (D + 2));      // [128][H2/2 + 1]
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(rtab) + kDecRowTabBytes);
   int* misc = reinterpret_cast<int*>(bars + 2 * S + 4);                  // abort flag, slot positions
   volatile int* abort_flag = misc;
@@ -188,12 +215,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 8);
+      mbar_init(empty(s), CW);
       tf[s * 18 + 16] = make_float2(1.0f, 0.0f);  // identity factor for unrotated dims
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(qfull(i), 1);
-      mbar_init(qempty(i), 8);
+      mbar_init(qempty(i), CW);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -269,7 +296,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // =============================================================== consumers ====
     const int cw = warp - 1;                  // consumer warp 0..7
     const int l8 = lane & 7;                  // lane of the row group
-    const int grp = cw * 4 + (lane >> 3);     // row group: rows grp + 32 jj of every tile
+    const int grp = cw * 4 + (lane >> 3);     // row group: rows grp + NG jj of every tile
     const int h2 = SMALL_R ? H2 : (p.r >> 1);
     // lanes whose chunk 0 holds rotated dims (r = 8..32: chunks 0..r/8-1, all 8 dims)
     const bool rot_lane = SMALL_R && 8 * l8 < 2 * h2;
@@ -286,7 +313,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
     for (int u = 0; u < 4; ++u) qo[u] = rot_lane ? pair0(2 * u) / 2 : RQ - 1;
     if constexpr (SMALL_R && H2 > 0) {
-      for (int e = tid - 32; e < kRows * RQ; e += 256) {
+      for (int e = tid - 32; e < kRows * RQ; e += NCT) {
         const int row = e / RQ, q = e - row * RQ;
         float4 f = make_float4(1.0f, 1.0f, 0.0f, 0.0f);
         if (q < RQ - 1) {
@@ -295,7 +322,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         rtab[e] = f;
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      consumers_sync<NCT>();
     }
     // (cos, sin) of chunk-0 dims (2u, 2u + 1) of row `row`, packed over the two dims
     auto row_factor = [&](int row, int u, uint64_t& c2, uint64_t& s2) {
@@ -371,19 +398,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const bool whole = t * kRows + kRows - 1 < P;  // every row valid, none is the new token
         if (SMALL_R && whole) {
           // ---- a full tile of cached keys: all loads first, then packed fp32 math
-          LaneRow<D> kr[4];
+          LaneRow<D> kr[RPG];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) kr[jj].load(kt + (grp + 32 * jj) * (2 * D), l8);
-          float sc[4];
+          for (int jj = 0; jj < RPG; ++jj) kr[jj].load(kt + (grp + NG * jj) * (2 * D), l8);
+          float sc[RPG];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
+          for (int jj = 0; jj < RPG; ++jj) {
             uint64_t acc = 0;
 #pragma unroll
             for (int u = 0; u < NV / 2; ++u) {
               uint64_t coef;
               if (H2 > 0 && u < 4) {
                 uint64_t c2, s2;
-                row_factor(grp + 32 * jj, u, c2, s2);
+                row_factor(grp + NG * jj, u, c2, s2);
                 coef = ffma2(cb2[u], s2, fmul2(ca2[u], c2));
               } else
                 coef = f32x2_pack(zr[2 * u], zr[2 * u + 1]);
@@ -391,14 +418,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
             sc[jj] = f2lo(acc) + f2hi(acc);
           }
-          LaneRow<D> vr[4];
+          LaneRow<D> vr[RPG];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) vr[jj].load(vt + (grp + 32 * jj) * (2 * D), l8);
+          for (int jj = 0; jj < RPG; ++jj) vr[jj].load(vt + (grp + NG * jj) * (2 * D), l8);
 #pragma unroll
           for (int x = 1; x <= 4; x <<= 1)
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], x);
-          const float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+            for (int jj = 0; jj < RPG; ++jj) sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], x);
+          const float mx = dec_max<RPG>(sc);
           if (mx > m + 8.0f) {
             const float f = ex2_approx(m - mx);
             l *= f;
@@ -407,23 +434,23 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             for (int u = 0; u < NV / 2; ++u) o2[u] = fmul2(o2[u], f2);
             m = mx;
           }
-          float pw[4];
+          float pw[RPG];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) pw[jj] = ex2_approx(sc[jj] - m);
-          l += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+          for (int jj = 0; jj < RPG; ++jj) pw[jj] = ex2_approx(sc[jj] - m);
+          l += dec_sum<RPG>(pw);
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
+          for (int jj = 0; jj < RPG; ++jj) {
             const uint64_t pp = f32x2_pack(pw[jj], pw[jj]);
 #pragma unroll
             for (int u = 0; u < NV / 2; ++u) o2[u] = ffma2(vr[jj].pair(u), pp, o2[u]);
           }
         } else {
         // ---- general tile: masked rows past P, the new token's row, any rotary_dim
-        float sc[4];
-        LaneRow<D> kr[4];
+        float sc[RPG];
+        LaneRow<D> kr[RPG];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int row = grp + 32 * jj;
+        for (int jj = 0; jj < RPG; ++jj) {
+          const int row = grp + NG * jj;
           const int key = t * kRows + row;
           const bool use = whole || key <= P;
           const uint8_t* src = (!whole && key == P) ? reinterpret_cast<const uint8_t*>(sq + D) : kt + row * (2 * D);
@@ -465,14 +492,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           sc[jj] = a0 + a1;
         }
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < RPG; ++jj) {
           sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], 1);
           sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], 2);
           sc[jj] += __shfl_xor_sync(0xffffffffu, sc[jj], 4);
-          if (!whole && t * kRows + grp + 32 * jj > P) sc[jj] = -INFINITY;
+          if (!whole && t * kRows + grp + NG * jj > P) sc[jj] = -INFINITY;
         }
         // online softmax of the group's rows (log2 units), lazy rescale beyond 2^8
-        const float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        const float mx = dec_max<RPG>(sc);
         if (mx > m + 8.0f) {
           const float f = ex2_approx(m - mx);
           l *= f;
@@ -481,13 +508,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           for (int u = 0; u < NV / 2; ++u) o2[u] = fmul2(o2[u], f2);
           m = mx;
         }
-        float pw[4];
+        float pw[RPG];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) pw[jj] = sc[jj] == -INFINITY ? 0.0f : ex2_approx(sc[jj] - m);
-        l += (pw[0] + pw[1]) + (pw[2] + pw[3]);
+        for (int jj = 0; jj < RPG; ++jj) pw[jj] = sc[jj] == -INFINITY ? 0.0f : ex2_approx(sc[jj] - m);
+        l += dec_sum<RPG>(pw);
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int row = grp + 32 * jj;
+        for (int jj = 0; jj < RPG; ++jj) {
+          const int row = grp + NG * jj;
           const int key = t * kRows + row;
           if (whole || key <= P) {
             const bool is_new = !whole && key == P;
@@ -522,7 +549,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(qempty(slot));  // and with the item slot
 
-      // ---- merge the 32 row groups: the warp's 4 groups by shuffles, then the 8 warps
+      // ---- merge the row groups: the warp's 4 groups by shuffles, then the CW warps
 #pragma unroll
       for (int x = 8; x <= 16; x <<= 1) {
         const float mo = __shfl_xor_sync(0xffffffffu, m, x), lo2 = __shfl_xor_sync(0xffffffffu, l, x);
@@ -538,7 +565,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         m = M;
       }
-      float* rb = red + ((k & 1) * 8 + cw) * (D + 2);
+      float* rb = red + ((k & 1) * CW + cw) * (D + 2);
       if (lane < 8) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) rb[lane_dim<D>(l8, v)] = (v & 1) ? f2hi(o2[v >> 1]) : f2lo(o2[v >> 1]);
@@ -547,16 +574,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         rb[D] = m;
         rb[D + 1] = l;
       }
-      const bool stop = consumers_sync_or(!ok || *abort_flag != 0);
+      const bool stop = consumers_sync_or<NCT>(!ok || *abort_flag != 0);
       if (stop) break;
       const int c = tid - 32;
       float M = -INFINITY, acc = 0.0f, L = 0.0f;
       if (c < D) {
-        const float* r0 = red + (k & 1) * 8 * (D + 2);
+        const float* r0 = red + (k & 1) * CW * (D + 2);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) M = fmaxf(M, r0[w * (D + 2) + D]);
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, r0[w * (D + 2) + D]);
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
+        for (int w = 0; w < CW; ++w) {
           const float mw = r0[w * (D + 2) + D];
           const float f = mw == -INFINITY ? 0.0f : ex2_approx(mw - M);
           acc = fmaf(r0[w * (D + 2) + c], f, acc);
@@ -580,13 +607,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           }
           __threadfence();
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        consumers_sync<NCT>();
         if (c == 0) {
           const bool last = atomicAdd(p.counters + head, 1) == runs - 1;
           if (last) p.counters[head] = 0;  // every run has arrived: ready for the next call
           *last_flag = last ? 1 : 0;
         }
-        asm volatile("bar.sync 1, 256;" ::: "memory");
+        consumers_sync<NCT>();
         if (*last_flag && c < D) {
           __threadfence();
           float Mh = -INFINITY;

@@ -299,7 +299,7 @@ int launch_decode_h2(const neox::DecodeParams& p, int ctas, cudaStream_t stream)
   cudaError_t e = cudaFuncSetAttribute(neox::attn_decode_kernel<D, H2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  neox::attn_decode_kernel<D, H2><<<ctas, neox::kDecThreads, smem, stream>>>(p);
+  neox::attn_decode_kernel<D, H2><<<ctas, neox::dec_threads(D), smem, stream>>>(p);
   e = cudaGetLastError();
   return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
 }
