@@ -55,6 +55,8 @@ def _load():
             lib.neox_oracle_probs.restype = i32
             lib.neox_oracle_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f64, P, P, i32]
             lib.neox_oracle_decode.restype = i32
+            lib.neox_oracle_bwd.argtypes = [P, P, i32, i32, i32, i32, i32, f64, P, i32]
+            lib.neox_oracle_bwd.restype = i32
             _lib = lib
     return _lib
 
@@ -154,3 +156,20 @@ def decode(qkv_new_bits: np.ndarray, k_cache_bits, v_cache_bits, pos, B: int, H:
     if rc != 0:
         raise ValueError(f"oracle decode failed ({rc})")
     return out, lse
+
+
+def bwd(qkv_bits: np.ndarray, dout_bits: np.ndarray, B: int, S: int, H: int, D: int, rotary_dim: int,
+        base: float = 10000.0, threads: int | None = None) -> np.ndarray:
+    """Gradient of sum(dout * out) with respect to the packed qkv, out being the forward.
+
+    qkv_bits: bf16 bits [B,S,H,3,D]; dout_bits: bf16 bits [B,S,H,D].
+    Returns dqkv fp64 [B,S,H,3,D] (slot 0 = dq, 1 = dk, 2 = dv), exact in fp64.
+    """
+    q = _u16(qkv_bits, (B, S, H, 3, D))
+    g = _u16(dout_bits, (B, S, H, D))
+    dqkv = np.zeros((B, S, H, 3, D), dtype=np.float64)
+    rc = _load().neox_oracle_bwd(_ptr(q), _ptr(g), B, S, H, D, rotary_dim, float(base), _ptr(dqkv),
+                                 threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle backward failed ({rc})")
+    return dqkv

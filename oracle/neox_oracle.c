@@ -31,6 +31,8 @@
  * softmax and no fusion:  widen bf16 -> fp64;  inv_freq;  rotate q_s and k_s by
  * angle s*inv_freq;  scores q'_i.k'_j / sqrt(D) for j <= i;  max;  exp;  sum;
  * weighted sum of v_j;  lse = max + ln(sum).
+ * The backward (neox_oracle_bwd, at the end) applies the chain rule to those same
+ * steps, in reverse, for the gradient of sum(dout * out) with respect to qkv.
  */
 #include <math.h>
 #include <pthread.h>
@@ -417,6 +419,161 @@ int neox_oracle_decode(const uint16_t* qkv_new, const uint16_t* k_cache, const u
   for (int t = 1; t < threads; ++t)
     if (pthread_create(&tid[started], NULL, worker_decode, &J) == 0) ++started;
   worker_decode(&J);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&J.mu);
+  return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------- backward ----
+ * Gradients of the loss L = sum(dout * out) with respect to the packed qkv, where
+ * out is the forward above.  The chain rule through each step of the forward, in
+ * its order ("gpt-neox - 模型与框架" page, section "问题二：注意力计算太慢", names the
+ * exact attention being differentiated; the rotation is the same rotate-half map):
+ *   p_ij = softmax_j(s_ij), s_ij = q'_i.k'_j / sqrt(D)  (j <= i),  o_i = sum_j p_ij v_j
+ *   dv_j  = sum_{i >= j} p_ij dout_i
+ *   dp_ij = dout_i . v_j,   delta_i = dout_i . o_i = sum_j p_ij dp_ij
+ *   ds_ij = p_ij (dp_ij - delta_i)          (softmax Jacobian applied to dp)
+ *   dq'_i = sum_j ds_ij k'_j / sqrt(D),   dk'_j = sum_{i >= j} ds_ij q'_i / sqrt(D)
+ *   dq_i = R(i)^T dq'_i,  dk_j = R(j)^T dk'_j  (R(p)^T is the rotation by -p theta).
+ * o_i and delta_i are recomputed here in fp64, not taken from a forward pass.   */
+typedef struct {
+  const uint16_t* qkv;
+  const uint16_t* dout;
+  int B, S, H, D, r;
+  double base;
+  double* dqkv;
+  pthread_mutex_t mu;
+  int64_t next, n_items;
+  int failed;
+} bjob_t;
+
+static void* worker_bwd(void* arg) {
+  bjob_t* J = (bjob_t*)arg;
+  const int S = J->S, H = J->H, D = J->D;
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  double* Qr = malloc(sizeof(double) * (size_t)S * D);
+  double* Kr = malloc(sizeof(double) * (size_t)S * D);
+  double* V = malloc(sizeof(double) * (size_t)S * D);
+  double* dO = malloc(sizeof(double) * (size_t)S * D);
+  double* dQr = malloc(sizeof(double) * (size_t)S * D);
+  double* dKr = malloc(sizeof(double) * (size_t)S * D);
+  double* dV = malloc(sizeof(double) * (size_t)S * D);
+  double* p = malloc(sizeof(double) * (size_t)S);
+  double* dp = malloc(sizeof(double) * (size_t)S);
+  double* tmp = malloc(sizeof(double) * (size_t)D);
+  double* o = malloc(sizeof(double) * (size_t)D);
+  if (!Qr || !Kr || !V || !dO || !dQr || !dKr || !dV || !p || !dp || !tmp || !o) {
+    pthread_mutex_lock(&J->mu);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->mu);
+  } else {
+    for (;;) {
+      pthread_mutex_lock(&J->mu);
+      int64_t item = J->next < J->n_items ? J->next++ : -1;
+      pthread_mutex_unlock(&J->mu);
+      if (item < 0) break;
+      const int64_t b = item / H, h = item % H;
+      for (int64_t s = 0; s < S; ++s) {
+        const uint16_t* qs = J->qkv + qkv_off(b, s, h, 0, S, H, D);
+        const uint16_t* ks = J->qkv + qkv_off(b, s, h, 1, S, H, D);
+        const uint16_t* vs = J->qkv + qkv_off(b, s, h, 2, S, H, D);
+        const uint16_t* g = J->dout + ((b * S + s) * H + h) * (int64_t)D;
+        for (int d = 0; d < D; ++d) tmp[d] = bf16_to_f64(qs[d]);
+        neox_oracle_rotate(tmp, D, J->r, J->base, s, Qr + s * D);
+        for (int d = 0; d < D; ++d) tmp[d] = bf16_to_f64(ks[d]);
+        neox_oracle_rotate(tmp, D, J->r, J->base, s, Kr + s * D);
+        for (int d = 0; d < D; ++d) {
+          V[s * D + d] = bf16_to_f64(vs[d]);
+          dO[s * D + d] = bf16_to_f64(g[d]);
+        }
+      }
+      memset(dQr, 0, sizeof(double) * (size_t)S * D);
+      memset(dKr, 0, sizeof(double) * (size_t)S * D);
+      memset(dV, 0, sizeof(double) * (size_t)S * D);
+      for (int64_t i = 0; i < S; ++i) {
+        /* forward row i: probabilities and output */
+        double m = -INFINITY;
+        for (int64_t j = 0; j <= i; ++j) {
+          double dot = 0.0;
+          for (int d = 0; d < D; ++d) dot += Qr[i * D + d] * Kr[j * D + d];
+          p[j] = dot * inv_sqrt_d;
+          if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j <= i; ++j) {
+          p[j] = exp(p[j] - m);
+          l += p[j];
+        }
+        for (int64_t j = 0; j <= i; ++j) p[j] /= l;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        for (int64_t j = 0; j <= i; ++j)
+          for (int d = 0; d < D; ++d) o[d] += p[j] * V[j * D + d];
+        /* backward of row i */
+        double delta = 0.0;
+        for (int d = 0; d < D; ++d) delta += dO[i * D + d] * o[d];
+        for (int64_t j = 0; j <= i; ++j) {
+          double acc = 0.0;
+          for (int d = 0; d < D; ++d) acc += dO[i * D + d] * V[j * D + d];
+          dp[j] = acc;
+          for (int d = 0; d < D; ++d) dV[j * D + d] += p[j] * dO[i * D + d];
+        }
+        for (int64_t j = 0; j <= i; ++j) {
+          const double ds = p[j] * (dp[j] - delta) * inv_sqrt_d;
+          for (int d = 0; d < D; ++d) {
+            dQr[i * D + d] += ds * Kr[j * D + d];
+            dKr[j * D + d] += ds * Qr[i * D + d];
+          }
+        }
+      }
+      /* back through the rotation: R(s)^T = R(-s) */
+      for (int64_t s = 0; s < S; ++s) {
+        double* gq = J->dqkv + qkv_off(b, s, h, 0, S, H, D);
+        double* gk = J->dqkv + qkv_off(b, s, h, 1, S, H, D);
+        double* gv = J->dqkv + qkv_off(b, s, h, 2, S, H, D);
+        neox_oracle_rotate(dQr + s * D, D, J->r, J->base, -s, gq);
+        neox_oracle_rotate(dKr + s * D, D, J->r, J->base, -s, gk);
+        for (int d = 0; d < D; ++d) gv[d] = dV[s * D + d];
+      }
+    }
+  }
+  free(Qr);
+  free(Kr);
+  free(V);
+  free(dO);
+  free(dQr);
+  free(dKr);
+  free(dV);
+  free(p);
+  free(dp);
+  free(tmp);
+  free(o);
+  return NULL;
+}
+
+/* dqkv: fp64 [B,S,H,3,D], every element written.  dout: bf16 bits [B,S,H,D]. */
+int neox_oracle_bwd(const uint16_t* qkv, const uint16_t* dout, int B, int S, int H, int D, int r, double base,
+                    double* dqkv, int threads) {
+  if (check_args(qkv, B, S, H, D, r, base) != ORACLE_OK || !dout || !dqkv) return ORACLE_ERR_ARG;
+  bjob_t J;
+  memset(&J, 0, sizeof J);
+  J.qkv = qkv;
+  J.dout = dout;
+  J.B = B;
+  J.S = S;
+  J.H = H;
+  J.D = D;
+  J.r = r;
+  J.base = base;
+  J.dqkv = dqkv;
+  J.n_items = (int64_t)B * H;
+  pthread_mutex_init(&J.mu, NULL);
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pthread_t tid[256];
+  int started = 0;
+  for (int t = 0; t < threads; ++t)
+    if (pthread_create(&tid[t], NULL, worker_bwd, &J) == 0) ++started;
+  if (started == 0) worker_bwd(&J);
   for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
   pthread_mutex_destroy(&J.mu);
   return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
