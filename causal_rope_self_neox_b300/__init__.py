@@ -27,7 +27,7 @@ NEOX_ERR_DEVICE_BAD_POSITION = -8
 
 EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
            "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
-           "neox_attn_version", "neox_attn_fwd_noalloc", "neox_attn_decode")
+           "neox_attn_version", "neox_attn_fwd_noalloc", "neox_attn_decode", "neox_attn_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -54,6 +54,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                 getattr(lib, name).restype = i32
             lib.neox_attn_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
             lib.neox_attn_decode.restype = i32
+            lib.neox_attn_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P]
+            lib.neox_attn_bwd.restype = i32
             lib.neox_attn_get_device_error.argtypes = []
             lib.neox_attn_get_device_error.restype = i32
             lib.neox_attn_status_string.argtypes = [i32]
@@ -98,6 +100,13 @@ def neox_attn_decode(qkv_new_ptr: int, k_cache_ptr: int, v_cache_ptr: int, pos_p
     """Raw call of the incremental decode (one new token per sequence against a K/V cache)."""
     return load_library().neox_attn_decode(qkv_new_ptr, k_cache_ptr, v_cache_ptr, pos_ptr, B, H, Smax, D, rotary_dim,
                                            rotary_base, out_ptr, lse_ptr, stream)
+
+
+def neox_attn_bwd(qkv_ptr: int, out_ptr: int, lse_ptr: int, dout_ptr: int, B: int, S: int, H: int, D: int,
+                  rotary_dim: int, rotary_base: float, dqkv_ptr: int, stream: int = 0) -> int:
+    """Raw call of the backward (dq, dk, dv of the packed qkv from dout and the forward's out, lse)."""
+    return load_library().neox_attn_bwd(qkv_ptr, out_ptr, lse_ptr, dout_ptr, B, S, H, D, rotary_dim, rotary_base,
+                                        dqkv_ptr, stream)
 
 
 def neox_attn_get_device_error() -> int:
@@ -194,6 +203,33 @@ def attn_decode(qkv_new, k_cache, v_cache, pos, rotary_dim: int, rotary_base: fl
     if rc != NEOX_OK:
         raise NeoxAttnError(rc, "neox_attn_decode")
     return out, lse
+
+
+def attn_bwd(qkv, out, lse, dout, rotary_dim: int, rotary_base: float = 10000.0, dqkv=None, stream=None):
+    """Backward on CUDA tensors: ``qkv`` bf16 ``[B,S,H,3,D]``, the forward's ``out`` bf16
+    ``[B,S,H,D]`` and ``lse`` fp32 ``[B,H,S]``, ``dout`` bf16 ``[B,S,H,D]``.  Returns
+    ``dqkv`` bf16 ``[B,S,H,3,D]`` (slot 0 = dq, 1 = dk, 2 = dv)."""
+    import torch
+
+    if qkv.dim() != 5 or qkv.shape[3] != 3 or qkv.dtype != torch.bfloat16 or not qkv.is_cuda:
+        raise ValueError("qkv must be a CUDA bf16 tensor of shape [B, S, H, 3, D]")
+    B, S, H, _, D = qkv.shape
+    for t, shape, dt in ((out, (B, S, H, D), torch.bfloat16), (dout, (B, S, H, D), torch.bfloat16),
+                         (lse, (B, H, S), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"expected a contiguous CUDA {dt} tensor of shape {list(shape)}")
+    if not qkv.is_contiguous():
+        raise ValueError("qkv must be contiguous")
+    if dqkv is None:
+        dqkv = torch.empty_like(qkv)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device)
+    with torch.cuda.device(qkv.device):
+        rc = neox_attn_bwd(qkv.data_ptr(), out.data_ptr(), lse.data_ptr(), dout.data_ptr(), B, S, H, D, rotary_dim,
+                           float(rotary_base), dqkv.data_ptr(), stream.cuda_stream)
+    if rc != NEOX_OK:
+        raise NeoxAttnError(rc, "neox_attn_bwd")
+    return dqkv
 
 
 def check_device_error() -> None:

@@ -16,6 +16,7 @@
 #include "attn_simple.cuh"
 #include "attn_ws.cuh"
 #include "decode.cuh"
+#include "attn_bwd.cuh"
 
 namespace {
 
@@ -354,6 +355,42 @@ int noalloc_table_address(int device, float2** out) {
   return NEOX_OK;
 }
 
+// ------------------------------------------------------------------ backward ----
+int validate_bwd(const void* qkv, const void* out, const float* lse, const void* dout, int B, int S, int H, int D,
+                 int r, float base, const void* dqkv) {
+  int rc = validate(qkv, B, S, H, D, r, base, out, lse);
+  if (rc != NEOX_OK) return rc;
+  if (!dout || !dqkv) return NEOX_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dout) & 15) || (reinterpret_cast<uintptr_t>(dqkv) & 15)) return NEOX_ERR_MISALIGNED;
+  const uint64_t rows = static_cast<uint64_t>(B) * S * H;
+  const uintptr_t g = reinterpret_cast<uintptr_t>(dout), d = reinterpret_cast<uintptr_t>(dqkv);
+  const uint64_t gb = rows * D * 2, db = rows * 3 * D * 2;
+  // dqkv is written: it may overlap no input; dout may alias nothing written either
+  if (ranges_overlap(d, db, reinterpret_cast<uintptr_t>(qkv), db) ||
+      ranges_overlap(d, db, reinterpret_cast<uintptr_t>(out), rows * D * 2) ||
+      ranges_overlap(d, db, reinterpret_cast<uintptr_t>(lse), static_cast<uint64_t>(B) * H * S * 4) ||
+      ranges_overlap(d, db, g, gb))
+    return NEOX_ERR_INVALID_ARG;
+  return NEOX_OK;
+}
+
+template <int D>
+int launch_bwd(const neox::BwdParams& p, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(p.B) * p.S * p.H;
+  neox::attn_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int smem = neox::bwd_smem_bytes(D);
+  e = cudaFuncSetAttribute(neox::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long ctas = static_cast<long long>(p.nblk) * p.B * p.H;
+  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), 128, smem, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -444,6 +481,56 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
       case 64: return launch_decode<64>(p, rotary_dim, ctas, stream);
       case 96: return launch_decode<96>(p, rotary_dim, ctas, stream);
       default: return launch_decode<128>(p, rotary_dim, ctas, stream);
+    }
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
+
+int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void* dout, int B, int S, int H, int D,
+                  int rotary_dim, float rotary_base, void* dqkv, void* stream_) {
+  try {
+    int rc = validate_bwd(qkv, out, lse, dout, B, S, H, D, rotary_dim, rotary_base, dqkv);
+    if (rc != NEOX_OK) return rc;
+    const long long nblk = (static_cast<long long>(S) + neox::kRows - 1) / neox::kRows;
+    if (nblk * B * H > 0x7FFFFFFFll) return NEOX_ERR_INVALID_ARG;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int device = 0;
+    DeviceInfo dev;
+    rc = current_device(&device, &dev);
+    if (rc != NEOX_OK) return rc;
+    const float2* cs = nullptr;
+    if (rotary_dim > 0) {
+      rc = get_table(device, S, rotary_dim, rotary_base, stream, &cs);
+      if (rc != NEOX_OK) return rc;
+    }
+    // scratch: the fp32 dq' accumulator [B,S,H,D], then delta [B,H,S]
+    const size_t rows = static_cast<size_t>(B) * S * H;
+    float* scratch = nullptr;
+    int* counters = nullptr;
+    rc = get_scratch(device, rows * D * sizeof(float) + rows * sizeof(float), 1, &scratch, &counters);
+    if (rc != NEOX_OK) return rc;
+    neox::BwdParams p{};
+    p.qkv = static_cast<const uint16_t*>(qkv);
+    p.out = static_cast<const uint16_t*>(out);
+    p.lse = lse;
+    p.dout = static_cast<const uint16_t*>(dout);
+    p.dqkv = static_cast<uint16_t*>(dqkv);
+    p.dq_acc = scratch;
+    p.delta = scratch + rows * D;
+    p.cs = cs;
+    p.B = B;
+    p.S = S;
+    p.H = H;
+    p.r = rotary_dim;
+    p.nblk = static_cast<int>(nblk);
+    p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
+    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    p.wait_limit_ns = neox::kWaitLimitNs;
+    switch (D) {
+      case 64: return launch_bwd<64>(p, stream);
+      case 96: return launch_bwd<96>(p, stream);
+      default: return launch_bwd<128>(p, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;

@@ -159,6 +159,36 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
                      int D, int rotary_dim, float rotary_base, void* out, float* lse, void* stream);
 
 /*
+ * Backward of neox_attn_fwd: the gradients of sum(dout * out) with respect to the
+ * packed projection.
+ *
+ * GPT-NeoX is a training framework that runs its attention as the exact, tiled
+ * Flash Attention ("gpt-neox - 模型与框架" page, section "问题二：注意力计算太慢");
+ * the pages print no backward, so the interface is the library's own and follows the
+ * chain rule through the forward: with p_ij = exp(s_ij - lse_i) over keys j <= i,
+ * dv_j = sum_i p_ij dout_i, ds_ij = p_ij (dout_i.v_j - dout_i.out_i),
+ * dq'_i = sum_j ds_ij k'_j / sqrt(D), dk'_j = sum_i ds_ij q'_i / sqrt(D), and dq, dk are
+ * dq', dk' rotated back (rotation by -theta on the first rotary_dim dims).
+ *
+ *   qkv          device, bf16 [B, S, H, 3, D], the forward's input; read only.
+ *   out, lse     device, the forward's outputs for this qkv (bf16 [B, S, H, D], 16-byte
+ *                aligned; fp32 [B, H, S], natural log, 4-byte aligned); read only.
+ *   dout         device, bf16 [B, S, H, D], 16-byte aligned; read only.
+ *   B, S, H, D, rotary_dim, rotary_base   as for neox_attn_fwd.
+ *   dqkv         device, bf16 [B, S, H, 3, D] (slot 0 = dq, 1 = dk, 2 = dv), 16-byte
+ *                aligned, written completely; may not overlap any input.
+ *   stream       a cudaStream_t (NULL = legacy default stream).
+ *
+ * Arithmetic: rotated q', k', the probabilities and ds enter the tensor cores as bf16,
+ * everything accumulates in fp32.  Ownership and errors as for neox_attn_fwd.  The
+ * library's per-device scratch (shared with neox_attn_decode, grown on demand, freed by
+ * neox_attn_release) holds an fp32 dq' accumulator of B*S*H*D and B*H*S floats, so
+ * backward and decode calls must not overlap on the GPU.
+ */
+int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void* dout, int B, int S, int H, int D,
+                  int rotary_dim, float rotary_base, void* dqkv, void* stream);
+
+/*
  * Reads and clears the current device's error word written by the kernels' bounded
  * waits and input checks.  Call after synchronizing the streams that ran the kernels.
  * Returns NEOX_OK, NEOX_ERR_DEVICE_TIMEOUT, NEOX_ERR_DEVICE_BAD_POSITION (decode
