@@ -84,6 +84,7 @@ def load_peaks():
 
 FWD_KERNEL_SOURCES = ("attn_ws.cuh", "attn_common.cuh", "ptx.cuh", "rotary.cuh", "tile_layout.cuh")
 DEC_KERNEL_SOURCES = ("decode.cuh", "attn_common.cuh", "ptx.cuh", "tile_layout.cuh", "neox_attn.cu")
+BWD_KERNEL_SOURCES = ("attn_bwd.cuh", "attn_common.cuh", "ptx.cuh", "tile_layout.cuh", "neox_attn.cu")
 
 
 def kernel_source_hash(sources=FWD_KERNEL_SOURCES) -> str:
@@ -411,6 +412,121 @@ def run_ours(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ backward ----
+BWD_METRIC = "causal NeoX-rotary attention backward TFLOP/s (5 B H S^2 D algorithmic FLOPs per step)"
+
+
+def run_bwd(args, w):
+    """One step = one neox_attn_bwd call (delta, the tcgen05 backward kernel, dq rotation
+    back) on the workload, with the forward's out and lse and a seeded dout resident."""
+    import torch
+    import causal_rope_self_neox_b300 as na
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0  # one GPU: the backward line is a single-replica measurement
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    qkv_cpu = make_qkv(w.B, w.S, w.H, w.D, w.seed, w.k_scale)
+    g = torch.Generator().manual_seed(w.seed + 7)
+    dout_cpu = torch.randn((w.B, w.S, w.H, w.D), generator=g).to(torch.bfloat16)
+    qkv, dout = qkv_cpu.to(dev), dout_cpu.to(dev)
+    out, lse = na.attn_fwd(qkv, w.rotary_dim, w.rotary_base)
+    dqkv = torch.empty_like(qkv)
+    flush = L2Flush(torch, dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flops = 2.5 * w.flops  # five S^2 D contractions over the causal half, against the forward's two
+
+    def step(q=qkv, o=out, l_=lse, gg=dout):
+        rc = na.neox_attn_bwd(q.data_ptr(), o.data_ptr(), l_.data_ptr(), gg.data_ptr(), w.B, w.S, w.H, w.D,
+                              w.rotary_dim, w.rotary_base, dqkv.data_ptr(), sh)
+        if rc != 0:
+            raise na.NeoxAttnError(rc, "neox_attn_bwd")
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    na.check_device_error()
+    if not bool(torch.isfinite(dqkv.float()).all()):
+        raise RuntimeError("non-finite gradients after warm-up")
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = "0"
+    try:
+        u = str(props.uuid)
+        gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as cs:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    clocks = cs.summary()
+    na.check_device_error()
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms_per_step = sum(ms) / len(ms)
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    # end to end: qkv, out, lse, dout in from pinned host memory, dqkv back
+    hq, ho, hl, hg = qkv_cpu.pin_memory(), out.cpu().pin_memory(), lse.cpu().pin_memory(), dout_cpu.pin_memory()
+    hd = torch.empty(dqkv.shape, dtype=dqkv.dtype).pin_memory()
+    dq_, do_, dl_, dg_ = torch.empty_like(qkv), torch.empty_like(out), torch.empty_like(lse), torch.empty_like(dout)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d_, h_ in ((dq_, hq), (do_, ho), (dl_, hl), (dg_, hg)):
+            d_.copy_(h_, non_blocking=True)
+        step(dq_, do_, dl_, dg_)
+        hd.copy_(dqkv, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    na.check_device_error()
+    peak, peak_sus, hbm, src = load_peaks()
+    traffic, tsrc = profiled_traffic(w.name, "attn_bwd", BWD_KERNEL_SOURCES)
+    line = {
+        "metric": BWD_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 qkv and dout)",
+        "config": {**w.describe(), "pass": "backward", "l2": L2_NOTE},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "traffic": traffic, "traffic_source": tsrc,
+                     "peak_kind": f"{src} dense bf16 burst (cuBLAS, kernel timed alone)",
+                     "kernel": f"attn_bwd_kernel<D={w.D}> + delta + dq kernels (all in the timed step)",
+                     "algorithmic_flops_per_launch": flops},
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "e2e": {"value": flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, ho, hl, hg)),
+                "d2h_bytes_per_step": hd.numel() * 2, "steps": e2e_steps, "ms_per_step": e2e_ms,
+                "path": "pinned host qkv, out, lse, dout -> device, neox_attn_bwd (C ABI), dqkv -> pinned host"},
+        "gpu_launches": 3 * args.steps,
+        "wall_s_timed_region": wall,
+        "kernel_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        used = oracle.default_threads()
+        nh = min(w.H, used)  # one head per host thread, batch 0
+        q1 = qkv_cpu[:1, :, :nh].contiguous()
+        g1 = dout_cpu[:1, :, :nh].contiguous()
+        t0 = time.perf_counter()
+        oracle.bwd(bf16_bits(q1), bf16_bits(g1), 1, w.S, nh, w.D, w.rotary_dim, w.rotary_base, used)
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 2.5 * 2 * nh * w.S * w.S * w.D / secs / 1e12, "unit": "TFLOP/s",
+                                "cores": used, "kind": "oracle", "seconds": secs,
+                                "sample": f"{nh} of the {w.B * w.H} heads (batch 0), fp64, {used} threads"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------- decode workloads ----
 DECODE_METRIC = "incremental decode: KV-cache GB/s read per step (and tokens/s)"
 
@@ -535,6 +651,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS), default="neox20b")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time the backward (neox_attn_bwd) on a prefill workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -544,6 +662,11 @@ def main():
             return 0
         return run_decode(args, DECODE_WORKLOADS[args.workload])
     w = WORKLOADS[args.workload]
+    if args.pass_ == "bwd":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the backward line has no reference arm"}))
+            return 0
+        return run_bwd(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

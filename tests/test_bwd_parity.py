@@ -1,12 +1,12 @@
 """GPU parity of the backward (neox_attn_bwd) against the fp64 backward oracle, through
 the C ABI.  The forward's out and lse come from neox_attn_fwd on the same input.
 
-Tolerances per gradient slot (dq, dk, dv): max abs error <= 3e-2 and RMS error <= 8e-3
-of the reference's RMS.  They come from the kernel's rounding points (rotated q', k',
-the probabilities and ds rounded to bf16 before the tensor cores, outputs rounded to
-bf16, fp32 everywhere else): restating those roundings in fp64 on CPU gives max abs
-errors up to 1.4e-2 and relative RMS up to 3.6e-3 on these shapes
-(tests/test_tolerance_budget.py checks that margin).
+Tolerances per gradient slot (dq, dk, dv): max abs error <= 1.5e-2 of the slot's
+largest reference value, and RMS error <= 1e-2 of the reference's RMS.  They come from
+the kernel's rounding points (rotated q', k', the probabilities and ds rounded to bf16
+before the tensor cores, outputs rounded to bf16, fp32 everywhere else): restating
+those roundings in fp64 on CPU gives at most 6.0e-3 and 3.9e-3 on such shapes, and
+tests/test_tolerance_budget.py checks that they stay within half of each bound.
 """
 import numpy as np
 import pytest
@@ -17,7 +17,7 @@ from causal_rope_self_neox_b300.workloads import WORKLOADS, bf16_bits, make_qkv
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS, REL_RMS = 3e-2, 8e-3
+MAX_REL, REL_RMS = 1.5e-2, 1e-2
 
 
 def make_dout(B, S, H, D, seed):
@@ -40,9 +40,10 @@ def check(got, ref, what):
         e = got[..., slot, :] - ref[..., slot, :]
         rms_ref = np.sqrt((ref[..., slot, :] ** 2).mean())
         # a slot that is exactly zero by definition (dq, dk of a one-token sequence) has
-        # no scale for a relative error: there the absolute bound alone applies
+        # no scale for a relative error: there an absolute bound of 1e-4 applies
+        bound = max(MAX_REL * np.abs(ref[..., slot, :]).max(), 1e-4)
         mx, rel = np.abs(e).max(), (np.sqrt((e ** 2).mean()) / rms_ref if rms_ref > 1e-6 else 0.0)
-        assert mx <= MAX_ABS and rel <= REL_RMS, (what, name, mx, rel)
+        assert mx <= bound and rel <= REL_RMS, (what, name, mx, bound, rel)
 
 
 @pytest.mark.parametrize("B,S,H,D,r", [

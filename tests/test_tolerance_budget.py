@@ -106,3 +106,59 @@ def test_split_scheme_fits_tolerances(name):
 def test_plain_bf16_rotation_breaks_lse_tolerance():
     _, _, lmax = errors(*CASES["tiny"], split=False)
     assert lmax > LSE_MAX, lmax
+
+
+# ------------------------------------------------------------------- backward ----
+# The backward kernel rounds the rotated q', k' to bf16 once (no hi/lo split), rounds the
+# probabilities P and ds to bf16 before its MMAs, takes delta from the forward's bf16
+# out and the fp32 lse, and writes bf16 gradients; everything else is fp32.  Restating
+# those rounding points in fp64 must stay well inside the GPU test's tolerances.
+BWD_MAX_REL, BWD_REL_RMS = 1.5e-2, 1e-2  # max abs error / max |ref|; RMS error / RMS ref
+
+
+def emulate_bwd(qkv, dout, r, base=10000.0):
+    """Gradients with the kernel's rounding points, fp64 elsewhere.  qkv, dout: fp64."""
+    B, S, H, _, D = qkv.shape
+    res = np.zeros((B, S, H, 3, D))
+    mask = np.tril(np.ones((S, S), dtype=bool))
+    h2 = r // 2
+    ang = np.arange(S)[:, None] * (base ** (-2.0 * np.arange(h2) / r))[None, :] if h2 else np.zeros((S, 0))
+    c, s = np.cos(ang), np.sin(ang)
+
+    def rot(x, sign):
+        y = x.copy()
+        y[:, :h2] = x[:, :h2] * c - sign * x[:, h2:r] * s
+        y[:, h2:r] = x[:, h2:r] * c + sign * x[:, :h2] * s
+        return y
+
+    for b in range(B):
+        for h in range(H):
+            q, k, v = rot(qkv[b, :, h, 0], 1), rot(qkv[b, :, h, 1], 1), qkv[b, :, h, 2]
+            g = dout[b, :, h]
+            sc = np.where(mask, q @ k.T / math.sqrt(D), -np.inf)
+            mx = sc.max(1, keepdims=True)
+            lse = (mx + np.log(np.exp(sc - mx).sum(1, keepdims=True)))[:, 0]
+            out = bf16_round(np.exp(sc - lse[:, None]) @ v)
+            qb, kb = bf16_round(q), bf16_round(k)
+            p = np.where(mask, np.exp(qb @ kb.T / math.sqrt(D) - np.float32(lse)[:, None]), 0.0)
+            ds = p * (g @ v.T - (g * out).sum(1)[:, None]) / math.sqrt(D)
+            pb, dsb = bf16_round(p), bf16_round(ds)
+            res[b, :, h, 0] = bf16_round(rot(dsb @ kb, -1))
+            res[b, :, h, 1] = bf16_round(rot(dsb.T @ qb, -1))
+            res[b, :, h, 2] = bf16_round(pb.T @ g)
+    return res
+
+
+@pytest.mark.parametrize("B,S,H,D,r", [(1, 300, 2, 64, 16), (1, 256, 2, 96, 24), (1, 200, 1, 128, 128),
+                                       (1, 129, 2, 128, 32), (1, 384, 1, 96, 6)])
+def test_bwd_rounding_points_fit_tolerances_with_margin(B, S, H, D, r):
+    import torch
+    qkv = make_qkv(B, S, H, D, seed=S + D + r)
+    dout = torch.randn((B, S, H, D), generator=torch.Generator().manual_seed(S + D + r + 7)).to(torch.bfloat16)
+    ref = oracle.bwd(bf16_bits(qkv), bf16_bits(dout), B, S, H, D, r)
+    got = emulate_bwd(qkv.to(torch.float64).numpy(), dout.to(torch.float64).numpy(), r)
+    for slot in range(3):
+        e = got[..., slot, :] - ref[..., slot, :]
+        rel = np.sqrt((e ** 2).mean()) / np.sqrt((ref[..., slot, :] ** 2).mean())
+        mrel = np.abs(e).max() / np.abs(ref[..., slot, :]).max()
+        assert mrel <= BWD_MAX_REL / 2 and rel <= BWD_REL_RMS / 2, (slot, mrel, rel)
