@@ -96,19 +96,29 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const BwdParams p) {
 
 // Rows [128 blk, 128 blk + 128) of one head of a row-major [B, S, H, stride] bf16 tensor
 // (head offset `col0` elements into the row) into a swizzled [128][D] tile; rows >= S
-// are zero.  Consecutive threads read consecutive 16-byte chunks of a row.
+// are zero.  Consecutive threads read consecutive 16-byte chunks of a row; every
+// thread's loads are issued before its first store (one memory latency per tile).
 template <int D>
 __device__ __forceinline__ void bwd_load_tile(uint8_t* tile, const uint16_t* base, long long row_stride, int col0,
                                               const BwdParams& p, int b, int h, int blk) {
   constexpr int CH = D / 8;
-  for (int idx = threadIdx.x; idx < kRows * CH; idx += blockDim.x) {
+  constexpr int PER = kRows * CH / 128;  // 128 threads
+  uint4 v[PER];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int idx = threadIdx.x + 128 * k;
     const int row = idx / CH, ch = idx - row * CH;
     const int s = blk * kRows + row;
-    uint4 v = make_uint4(0, 0, 0, 0);
+    v[k] = make_uint4(0, 0, 0, 0);
     if (s < p.S)
-      v = *reinterpret_cast<const uint4*>(base + ((static_cast<long long>(b) * p.S + s) * p.H + h) * row_stride +
-                                          col0 + ch * 8);
-    *reinterpret_cast<uint4*>(tile + sw64_off(row, ch * 8)) = v;
+      v[k] = *reinterpret_cast<const uint4*>(base + ((static_cast<long long>(b) * p.S + s) * p.H + h) * row_stride +
+                                             col0 + ch * 8);
+  }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    const int idx = threadIdx.x + 128 * k;
+    const int row = idx / CH, ch = idx - row * CH;
+    *reinterpret_cast<uint4*>(tile + sw64_off(row, ch * 8)) = v[k];
   }
 }
 
