@@ -94,47 +94,6 @@ __global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const BwdParams p) {
   }
 }
 
-// Rows [128 blk, 128 blk + 128) of one head of a row-major [B, S, H, stride] bf16 tensor
-// (head offset `col0` elements into the row) into a swizzled [128][D] tile; rows >= S
-// are zero.  Consecutive threads read consecutive 16-byte chunks of a row; every
-// thread's loads are issued before its first store (one memory latency per tile).
-template <int D>
-__device__ __forceinline__ void bwd_load_tile(uint8_t* tile, const uint16_t* base, long long row_stride, int col0,
-                                              const BwdParams& p, int b, int h, int blk) {
-  constexpr int CH = D / 8;
-  constexpr int PER = kRows * CH / 128;  // 128 threads
-  uint4 v[PER];
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int idx = threadIdx.x + 128 * k;
-    const int row = idx / CH, ch = idx - row * CH;
-    const int s = blk * kRows + row;
-    v[k] = make_uint4(0, 0, 0, 0);
-    if (s < p.S)
-      v[k] = *reinterpret_cast<const uint4*>(base + ((static_cast<long long>(b) * p.S + s) * p.H + h) * row_stride +
-                                             col0 + ch * 8);
-  }
-#pragma unroll
-  for (int k = 0; k < PER; ++k) {
-    const int idx = threadIdx.x + 128 * k;
-    const int row = idx / CH, ch = idx - row * CH;
-    *reinterpret_cast<uint4*>(tile + sw64_off(row, ch * 8)) = v[k];
-  }
-}
-
-// Rotate the first r dims of one tile row in place at position pos (rounded to bf16).
-__device__ __forceinline__ void bwd_rotate_row(uint8_t* tile, int row, long long pos, const float2* cs, int r) {
-  const int h2 = r >> 1;
-  for (int i = 0; i < h2; ++i) {
-    uint16_t* pa = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i));
-    uint16_t* pb = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i + h2));
-    const float x1 = bf16_bits_to_f32(*pa), x2 = bf16_bits_to_f32(*pb);
-    const float2 c = cs[pos * h2 + i];
-    *pa = f32_to_bf16_bits(fmaf(x1, c.x, -x2 * c.y));
-    *pb = f32_to_bf16_bits(fmaf(x2, c.x, x1 * c.y));
-  }
-}
-
 // kind::f16 instruction descriptor with the A major-ness as well (bit 15: 1 = MN-major).
 __host__ __device__ constexpr uint32_t idesc_bwd(int M, int N, bool a_mn, bool b_mn) {
   return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
@@ -145,93 +104,170 @@ __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c
                : "memory");
 }
 
-// smem: K'_j, V_j, Q'_i, dO_i tiles [128][D], P_i and dS_i tiles [128][128], a barrier,
-// the TMEM address and the abort flag (tiles 1 KB aligned).
-__host__ __device__ constexpr int bwd_smem_bytes(int D) { return 1024 + 4 * tile_bytes(D) + 2 * tile_bytes(128) + 64; }
+// Query-side buffers (Q'_i and dO_i tile pairs): two for D <= 96, so the next block's
+// tiles load (TMA) and rotate while the current block's MMAs run; one for D = 128, where
+// a second pair does not fit next to K', V, P and dS.
+__host__ __device__ constexpr int bwd_qbufs(int D) { return D == 128 ? 1 : 2; }
+// smem: K'_j, V_j, then per buffer Q'_i and dO_i, then P_i and dS_i [128][128] tiles
+// (1 KB aligned), barriers, the TMEM address and the abort flag.
+__host__ __device__ constexpr int bwd_smem_bytes(int D) {
+  return 1024 + (2 + 2 * bwd_qbufs(D)) * tile_bytes(D) + 2 * tile_bytes(128) + 128;
+}
+constexpr int kBwdThreads = 256;  // two threads per tile row (each half of the columns)
+
+// Rotate pairs part, part + 2, ... (< r/2) of one tile row in place at position pos,
+// rounded to bf16; the table entries of up to 8 pairs are loaded before they are used.
+__device__ __forceinline__ void bwd_rotate_row(uint8_t* tile, int row, long long pos, const float2* cs, int r,
+                                               int part) {
+  const int h2 = r >> 1;
+  for (int i0 = part; i0 < h2; i0 += 16) {
+    float2 c[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) c[e] = i0 + 2 * e < h2 ? cs[pos * h2 + i0 + 2 * e] : make_float2(1.0f, 0.0f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int i = i0 + 2 * e;
+      if (i < h2) {
+        uint16_t* pa = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i));
+        uint16_t* pb = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i + h2));
+        const float x1 = bf16_bits_to_f32(*pa), x2 = bf16_bits_to_f32(*pb);
+        *pa = f32_to_bf16_bits(fmaf(x1, c[e].x, -x2 * c[e].y));
+        *pb = f32_to_bf16_bits(fmaf(x2, c[e].x, x1 * c[e].y));
+      }
+    }
+  }
+}
 
 template <int D>
-__global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg,
+                    const BwdParams p) {
+  constexpr int NB = bwd_qbufs(D);
+  constexpr int TB = tile_bytes(D);
+  constexpr int DH = D / 2;  // output columns per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Kt = smem;
-  uint8_t* Vt = Kt + tile_bytes(D);
-  uint8_t* Qt = Vt + tile_bytes(D);
-  uint8_t* Gt = Qt + tile_bytes(D);
-  uint8_t* Pt = Gt + tile_bytes(D);
+  uint8_t* Vt = Kt + TB;
+  auto Qb = [&](int k) { return Vt + TB + 2 * k * TB; };
+  auto Gb = [&](int k) { return Vt + TB + (2 * k + 1) * TB; };
+  uint8_t* Pt = Vt + TB + 2 * NB * TB;
   uint8_t* St = Pt + tile_bytes(128);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(St + tile_bytes(128));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(St + tile_bytes(128));  // kv, ld[2], mma
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int row = tid & (kRows - 1), half = tid >> 7;
   const int BH = p.B * p.H;
   const int j = blockIdx.x / BH;  // key block; the heaviest (j = 0) blocks are launched first
   const int bh = blockIdx.x - j * BH;
   const int b = bh / p.H, h = bh - b * p.H;
-  const uint32_t bar_mma = smem_u32(bar);
+  const uint32_t bar_kv = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[3]);
+  auto bar_ld = [&](int k) { return smem_u32(&bars[1 + k]); };
+  const uint64_t lim = p.wait_limit_ns;
 
   if (tid == 0) {
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_ld(0), 1);
+    mbar_init(bar_ld(1), 1);
     mbar_init(bar_mma, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch_map(&tq);
+    tma_prefetch_map(&tg);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  // K'_j (rotated) and V_j
-  bwd_load_tile<D>(Kt, p.qkv, 3 * D, D, p, b, h, j);
-  bwd_load_tile<D>(Vt, p.qkv, 3 * D, 2 * D, p, b, h, j);
-  __syncthreads();
-  const long long key = static_cast<long long>(j) * kRows + tid;
-  if (p.r > 0 && key < p.S) bwd_rotate_row(Kt, tid, key, p.cs, p.r);
-  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-
   const uint32_t tbase = *tmem_slot;
   const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 256 + D, tdQ = tbase;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   constexpr uint32_t idesc_s = idesc_bwd(128, 128, false, false);  // S, dP
   constexpr uint32_t idesc_t = idesc_bwd(128, D, true, true);      // dV, dK: A = P^T / dS^T
   constexpr uint32_t idesc_q = idesc_bwd(128, D, false, true);     // dQ: A = dS, B = K'
-  uint32_t ph = 0;
-  bool pending = false;  // thread 0: an MMA commit not yet waited for
+
+  // thread 0 only: copies and MMAs in flight, for the abort path
+  bool kv_pending = false, mma_pending = false;
+  bool ld_pending[2] = {false, false};
+  uint32_t ph_ld[2] = {0, 0}, ph_mma = 0;
+  auto issue_qg = [&](int k, int blk) {  // Q_blk (raw) and dO_blk into buffer k
+    mbar_arrive_expect_tx(bar_ld(k), 2 * TB);
+    for (int cb = 0; cb < D / kBlkCols; ++cb) {
+      tma_load_4d(smem_u32(Qb(k) + cb * kBlkBytes), &tq, bar_ld(k), cb * kBlkCols, 3 * h + 0, blk * kRows, b);
+      tma_load_4d(smem_u32(Gb(k) + cb * kBlkBytes), &tg, bar_ld(k), cb * kBlkCols, h, blk * kRows, b);
+    }
+    ld_pending[k] = true;
+  };
+  // wait for buffer k's tiles, then rotate the query rows (pairs split between the halves)
+  auto land_and_rotate = [&](int k, int blk, unsigned int site) -> bool {
+    wait_phase(bar_ld(k), ph_ld[k], abort_flag, lim, site);
+    __syncthreads();
+    if (*abort_flag) return false;
+    ph_ld[k] ^= 1;
+    if (tid == 0) ld_pending[k] = false;
+    const long long q = static_cast<long long>(blk) * kRows + row;
+    if (p.r > 0 && q < p.S) bwd_rotate_row(Qb(k), row, q, p.cs, p.r, half);
+    return true;
+  };
+
   bool ok = true;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_kv, 2 * TB);
+    for (int cb = 0; cb < D / kBlkCols; ++cb) {
+      tma_load_4d(smem_u32(Kt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * h + 1, j * kRows, b);
+      tma_load_4d(smem_u32(Vt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * h + 2, j * kRows, b);
+    }
+    kv_pending = true;
+    issue_qg(0, j);
+  }
+  wait_phase(bar_kv, 0, abort_flag, lim, 42);
+  __syncthreads();
+  const long long key = static_cast<long long>(j) * kRows + row;
+  if (*abort_flag) {
+    ok = false;
+  } else {
+    if (tid == 0) kv_pending = false;
+    if (p.r > 0 && key < p.S) bwd_rotate_row(Kt, row, key, p.cs, p.r, half);
+    ok = land_and_rotate(0, j, 43);
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
 
   for (int i = j; i < p.nblk && ok; ++i) {
-    // ---- Q'_i (rotated) and dO_i
-    bwd_load_tile<D>(Qt, p.qkv, 3 * D, 0, p, b, h, i);
-    bwd_load_tile<D>(Gt, p.dout, D, 0, p, b, h, i);
-    __syncthreads();
-    const long long q = static_cast<long long>(i) * kRows + tid;
-    const bool qvalid = q < p.S;
-    if (p.r > 0 && qvalid) bwd_rotate_row(Qt, tid, q, p.cs, p.r);
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-
-    // ---- S = Q' K'^T, dP = dO V^T
+    const int bi = NB == 2 ? ((i - j) & 1) : 0;
+    const bool next = i + 1 < p.nblk;
+    // ---- next block's tiles into the other buffer (free: block i-1 is done), then
+    //      S = Q' K'^T and dP = dO V^T
     if (tid == 0) {
+      if (NB == 2 && next) issue_qg(bi ^ 1, i + 1);
       tc_fence_after_sync();
-      const uint32_t qa = smem_u32(Qt), ka = smem_u32(Kt), ga = smem_u32(Gt), va = smem_u32(Vt);
+      const uint32_t qa = smem_u32(Qb(bi)), ka = smem_u32(Kt), ga = smem_u32(Gb(bi)), va = smem_u32(Vt);
       for (int kc = 0; kc < D / 16; ++kc) mma_ss(tS, kmajor_desc(qa, kc), kmajor_desc(ka, kc), idesc_s, kc > 0);
       for (int kc = 0; kc < D / 16; ++kc) mma_ss(tdP, kmajor_desc(ga, kc), kmajor_desc(va, kc), idesc_s, kc > 0);
       tc_commit(bar_mma);
-      pending = true;
+      mma_pending = true;
     }
-    wait_phase(bar_mma, ph, abort_flag, p.wait_limit_ns, 40);
-    __syncthreads();
-    if (*abort_flag) { ok = false; break; }
-    ph ^= 1;
-    if (tid == 0) pending = false;
-    tc_fence_after_sync();
-
-    // ---- P = exp(S/sqrt(D) - lse), dS = P (dP - delta) / sqrt(D), both to smem as bf16
+    const long long q = static_cast<long long>(i) * kRows + row;
+    const bool qvalid = q < p.S;
+    // this row's lse and delta, loaded while the MMAs run
     const float lse2 = qvalid ? p.lse[(static_cast<long long>(b) * p.H + h) * p.S + q] * kLog2e : 0.0f;
     const float dl = qvalid ? p.delta[(static_cast<long long>(b) * p.H + h) * p.S + q] : 0.0f;
-    for (int c0 = 0; c0 < 128; c0 += 32) {
+    wait_phase(bar_mma, ph_mma, abort_flag, lim, 40);
+    __syncthreads();
+    if (*abort_flag) { ok = false; break; }
+    ph_mma ^= 1;
+    if (tid == 0) mma_pending = false;
+    tc_fence_after_sync();
+
+    // ---- P = exp(S/sqrt(D) - lse), dS = P (dP - delta) / sqrt(D) for this thread's 64
+    //      keys of the row, to shared memory as bf16
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
       uint32_t sr[32], dr[32];
       tmem_ld32(tS + lane_off + c0, sr);
       tmem_ld32(tdP + lane_off + c0, dr);
@@ -253,9 +289,9 @@ __global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p) {
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        *reinterpret_cast<uint4*>(Pt + sw64_off(tid, c0 + 8 * k)) =
+        *reinterpret_cast<uint4*>(Pt + sw64_off(row, c0 + 8 * k)) =
             make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        *reinterpret_cast<uint4*>(St + sw64_off(tid, c0 + 8 * k)) =
+        *reinterpret_cast<uint4*>(St + sw64_off(row, c0 + 8 * k)) =
             make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
       }
     }
@@ -266,57 +302,68 @@ __global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p) {
     // ---- dV += P^T dO, dK += dS^T Q' (accumulating over i), dQ'_i = dS K'
     if (tid == 0) {
       tc_fence_after_sync();
-      const uint32_t pa = smem_u32(Pt), sa = smem_u32(St), ga = smem_u32(Gt), qa = smem_u32(Qt), ka = smem_u32(Kt);
+      const uint32_t pa = smem_u32(Pt), sa = smem_u32(St), ga = smem_u32(Gb(bi)), qa = smem_u32(Qb(bi)),
+                     ka = smem_u32(Kt);
       for (int kk = 0; kk < kRows / 16; ++kk)
         mma_ss(tdV, vmajor_desc(pa, kk), vmajor_desc(ga, kk), idesc_t, (i > j || kk > 0) ? 1u : 0u);
       for (int kk = 0; kk < kRows / 16; ++kk)
         mma_ss(tdK, vmajor_desc(sa, kk), vmajor_desc(qa, kk), idesc_t, (i > j || kk > 0) ? 1u : 0u);
       for (int kc = 0; kc < kRows / 16; ++kc) mma_ss(tdQ, kmajor_desc(sa, kc), vmajor_desc(ka, kc), idesc_q, kc > 0);
       tc_commit(bar_mma);
-      pending = true;
+      mma_pending = true;
     }
-    wait_phase(bar_mma, ph, abort_flag, p.wait_limit_ns, 41);
+    // the next block's tiles land and rotate while these MMAs run
+    if (NB == 2 && next && !land_and_rotate(bi ^ 1, i + 1, 44)) { ok = false; break; }
+    wait_phase(bar_mma, ph_mma, abort_flag, lim, 41);
     __syncthreads();
     if (*abort_flag) { ok = false; break; }
-    ph ^= 1;
-    if (tid == 0) pending = false;
+    ph_mma ^= 1;
+    if (tid == 0) mma_pending = false;
     tc_fence_after_sync();
 
-    // ---- dq' rows of this query block into the fp32 accumulator
+    // ---- this thread's half of the dq' row into the fp32 accumulator
     float* dq = p.dq_acc + ((static_cast<long long>(b) * p.S + (qvalid ? q : 0)) * p.H + h) * D;
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tdQ + lane_off + c0, r);
+    for (int c0 = DH * half; c0 < DH * half + DH; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tdQ + lane_off + c0, r);
       tmem_wait_ld();
       if (qvalid) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 4)
+        for (int k = 0; k < 16; k += 4)
           red_add_v4(dq + c0 + k, __uint_as_float(r[k]), __uint_as_float(r[k + 1]), __uint_as_float(r[k + 2]),
                      __uint_as_float(r[k + 3]));
       }
     }
+    if (NB == 1 && next) {  // single buffer: the next block's tiles only now
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) issue_qg(0, i + 1);
+      if (!land_and_rotate(0, i + 1, 45)) { ok = false; break; }
+    }
+    fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
   }
 
-  // ---- dk = R(key)^T dk', dv: rows of key block j, bf16 into slots 1 and 2
+  // ---- dk = R(key)^T dk' and dv for the rows of key block j, bf16 into slots 1 and 2
   if (ok && !*abort_flag) {
     tc_fence_after_sync();
     const bool kvalid = key < p.S;
     uint16_t* dst = p.dqkv + ((static_cast<long long>(b) * p.S + (kvalid ? key : 0)) * p.H + h) * 3 * D;
-    // dk' row staged in shared memory (the Q'/dO/P/dS tiles are free now), one padded
-    // row per thread, so the rotation can pick its pair partners by index
-    float* xs = reinterpret_cast<float*>(Qt) + tid * (D + 1);
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tdK + lane_off + c0, r);
+    // dk' rows staged in shared memory (the query-side tiles are free now), padded rows,
+    // so the rotation can read the pair partners of the other half
+    float* xs = reinterpret_cast<float*>(Qb(0)) + row * (D + 1);
+    for (int c0 = DH * half; c0 < DH * half + DH; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tdK + lane_off + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) xs[c0 + k] = __uint_as_float(r[k]);
+      for (int k = 0; k < 16; ++k) xs[c0 + k] = __uint_as_float(r[k]);
     }
+    __syncthreads();
     const int h2 = p.r >> 1;
     if (kvalid) {
-      for (int d0 = 0; d0 < D; d0 += 8) {
+      for (int d0 = DH * half; d0 < DH * half + DH; d0 += 8) {
         float y[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -335,13 +382,13 @@ __global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p) {
                                                              pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
       }
     }
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tdV + lane_off + c0, r);
+    for (int c0 = DH * half; c0 < DH * half + DH; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(tdV + lane_off + c0, r);
       tmem_wait_ld();
       if (kvalid) {
 #pragma unroll
-        for (int k = 0; k < 32; k += 8)
+        for (int k = 0; k < 16; k += 8)
           *reinterpret_cast<uint4*>(dst + 2 * D + c0 + k) =
               make_uint4(pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
                          pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
@@ -351,8 +398,13 @@ __global__ void __launch_bounds__(128, 1) attn_bwd_kernel(const BwdParams p) {
     }
   }
 
-  // ---- teardown: let an MMA in flight land, then free TMEM
-  if (tid == 0 && pending) drain_phase(bar_mma, ph, p.wait_limit_ns);
+  // ---- teardown: let the copies and MMAs in flight land, then free TMEM
+  if (tid == 0) {
+    if (kv_pending) drain_phase(bar_kv, 0, lim);
+    for (int k = 0; k < 2; ++k)
+      if (ld_pending[k]) drain_phase(bar_ld(k), ph_ld[k], lim);
+    if (mma_pending) drain_phase(bar_mma, ph_mma, lim);
+  }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 0) {

@@ -128,7 +128,8 @@ int get_table(int device, int S, int r, float base, cudaStream_t stream, const f
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D) {
+// cuTensorMapEncodeTiled through the runtime's driver entry point, resolved once.
+bool resolve_encode() {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -136,7 +137,11 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D
         q == cudaDriverEntryPointSuccess)
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
-  if (!g_encode) return cuda_fail(cudaErrorNotSupported);
+  return g_encode != nullptr;
+}
+
+int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D) {
+  if (!resolve_encode()) return cuda_fail(cudaErrorNotSupported);
   // dims (innermost first): head dim, (head, slot), sequence, batch.
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(3) * H, static_cast<cuuint64_t>(S),
                         static_cast<cuuint64_t>(B)};
@@ -374,8 +379,25 @@ int validate_bwd(const void* qkv, const void* out, const float* lse, const void*
   return NEOX_OK;
 }
 
+// TMA view of a row-major [B, S, H, D] bf16 tensor (dout): dims {D, H, S, B}, the same
+// {32, 1, 128, 1} box and swizzle as the qkv view.
+int encode_rows_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int D) {
+  if (!resolve_encode()) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(S) * H * D * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(neox::kBlkCols), 1, static_cast<cuuint32_t>(neox::kRows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return NEOX_OK;
+}
+
 template <int D>
-int launch_bwd(const neox::BwdParams& p, cudaStream_t stream) {
+int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tg, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.S * p.H;
   neox::attn_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -384,7 +406,7 @@ int launch_bwd(const neox::BwdParams& p, cudaStream_t stream) {
   e = cudaFuncSetAttribute(neox::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   const long long ctas = static_cast<long long>(p.nblk) * p.B * p.H;
-  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), 128, smem, stream>>>(p);
+  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tg, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
   e = cudaGetLastError();
@@ -510,6 +532,11 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     int* counters = nullptr;
     rc = get_scratch(device, rows * D * sizeof(float) + rows * sizeof(float), 1, &scratch, &counters);
     if (rc != NEOX_OK) return rc;
+    CUtensorMap tq, tg;
+    rc = encode_qkv_map(&tq, qkv, B, S, H, D);
+    if (rc != NEOX_OK) return rc;
+    rc = encode_rows_map(&tg, dout, B, S, H, D);
+    if (rc != NEOX_OK) return rc;
     neox::BwdParams p{};
     p.qkv = static_cast<const uint16_t*>(qkv);
     p.out = static_cast<const uint16_t*>(out);
@@ -528,9 +555,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
     switch (D) {
-      case 64: return launch_bwd<64>(p, stream);
-      case 96: return launch_bwd<96>(p, stream);
-      default: return launch_bwd<128>(p, stream);
+      case 64: return launch_bwd<64>(p, tq, tg, stream);
+      case 96: return launch_bwd<96>(p, tq, tg, stream);
+      default: return launch_bwd<128>(p, tq, tg, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
