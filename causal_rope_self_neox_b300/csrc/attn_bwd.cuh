@@ -10,12 +10,13 @@
 //   dq'_i = sum_j ds_ij k'_j / sqrt(D)         dk'_j = sum_i ds_ij q'_i / sqrt(D)
 //   dq_i = R(i)^T dq'_i,  dk_j = R(j)^T dk'_j  (the rotation back by -theta).
 // Three kernels on the caller's stream:
-//   attn_bwd_delta_kernel  delta_i (fp32) and a zeroed fp32 dq' accumulator;
+//   attn_bwd_prep_kernel   the rotated q', k' (bf16, rounded once) with v into a scratch
+//                          copy of qkv, delta_i (fp32) and a zeroed fp32 dq' accumulator;
 //   attn_bwd_kernel        one CTA per (key block j, head): K'_j, V_j stay in shared
 //                          memory while query blocks i >= j stream through; per block
 //                          five tcgen05 MMAs (S = Q'K'^T and dP = dO V^T into TMEM, then
 //                          dV += P^T dO and dK += dS^T Q' accumulating in TMEM over i, and
-//                          dQ'_i = dS K' added to the fp32 accumulator with vector reds);
+//                          dQ'_i = dS K' added to the fp32 accumulator by bulk reductions);
 //                          at the end dk (rotated back) and dv are written as bf16;
 //   attn_bwd_dq_kernel     rotates the accumulated dq' back and writes dq as bf16.
 // P and dS enter the MMAs as bf16 (fp32 accumulation), as do the rotated q', k' (rounded
@@ -33,6 +34,7 @@ struct BwdParams {
   const float* lse;      // fp32 [B, H, S]     (the forward's, natural log)
   const uint16_t* dout;  // bf16 [B, S, H, D]
   uint16_t* dqkv;        // bf16 [B, S, H, 3, D]
+  uint16_t* qkv_rot;     // bf16 [B, S, H, 3, D]  scratch: rotated q', k' and v
   float* dq_acc;         // fp32 [B, S, H, D]  scratch: dq' before the rotation back
   float* delta;          // fp32 [B, H, S]     scratch
   const float2* cs;      // cos/sin table [>= S rows][r/2]
@@ -44,12 +46,33 @@ struct BwdParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// delta[b, h, s] = dout . out for every row (one warp per row), and dq_acc zeroed.
+// Per row (one warp per row): qkv_rot = (R(s) q, R(s) k, v) in bf16 (the rotation
+// rounded once, as the MMAs take it), delta = dout . out (fp32), and dq_acc zeroed.
+// Lane l handles dims l, l + 32, ...; a rotated dim reads its pair partner directly.
 template <int D>
-__global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // [b][s][h]
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<long long>(p.B) * p.S * p.H) return;
+  const long long s = (row / p.H) % p.S;
+  const int h2 = p.r >> 1;
+  const uint16_t* src = p.qkv + row * 3 * D;
+  uint16_t* dst = p.qkv_rot + row * 3 * D;
+  for (int d = lane; d < D; d += 32) {
+    float yq = bf16_bits_to_f32(src[d]), yk = bf16_bits_to_f32(src[D + d]);
+    if (d < p.r) {
+      const int i = d < h2 ? d : d - h2;
+      const int partner = d < h2 ? d + h2 : d - h2;
+      const float sg = d < h2 ? -1.0f : 1.0f;  // y_i = x_i c - x_{i+h} s,  y_{i+h} = x_{i+h} c + x_i s
+      const float2 c = p.cs[s * h2 + i];
+      const float pq = bf16_bits_to_f32(src[partner]), pk = bf16_bits_to_f32(src[D + partner]);
+      yq = fmaf(yq, c.x, sg * pq * c.y);
+      yk = fmaf(yk, c.x, sg * pk * c.y);
+    }
+    dst[d] = f32_to_bf16_bits(yq);
+    dst[D + d] = f32_to_bf16_bits(yk);
+    dst[2 * D + d] = src[2 * D + d];
+  }
   const uint16_t* o = p.out + row * D;
   const uint16_t* g = p.dout + row * D;
   float acc = 0.0f;
@@ -59,7 +82,7 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(const BwdParams p) 
   float* dq = p.dq_acc + row * D;
   for (int d = lane; d < D; d += 32) dq[d] = 0.0f;
   if (lane == 0) {
-    const long long h = row % p.H, s = (row / p.H) % p.S, b = row / (static_cast<long long>(p.H) * p.S);
+    const long long h = row % p.H, b = row / (static_cast<long long>(p.H) * p.S);
     p.delta[(b * p.H + h) * p.S + s] = acc;
   }
 }
@@ -99,11 +122,6 @@ __host__ __device__ constexpr uint32_t idesc_bwd(int M, int N, bool a_mn, bool b
   return idesc_bf16_f32(M, N, b_mn) | ((a_mn ? 1u : 0u) << 15);
 }
 
-__device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 // Query-side buffers (Q'_i and dO_i tile pairs): two for D <= 96, so the next block's
 // tiles load (TMA) and rotate while the current block's MMAs run; one for D = 128, where
 // a second pair does not fit next to K', V, P and dS.
@@ -115,28 +133,14 @@ __host__ __device__ constexpr int bwd_smem_bytes(int D) {
 }
 constexpr int kBwdThreads = 256;  // two threads per tile row (each half of the columns)
 
-// Rotate pairs part, part + 2, ... (< r/2) of one tile row in place at position pos,
-// rounded to bf16; the table entries of up to 8 pairs are loaded before they are used.
-__device__ __forceinline__ void bwd_rotate_row(uint8_t* tile, int row, long long pos, const float2* cs, int r,
-                                               int part) {
-  const int h2 = r >> 1;
-  for (int i0 = part; i0 < h2; i0 += 16) {
-    float2 c[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) c[e] = i0 + 2 * e < h2 ? cs[pos * h2 + i0 + 2 * e] : make_float2(1.0f, 0.0f);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int i = i0 + 2 * e;
-      if (i < h2) {
-        uint16_t* pa = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i));
-        uint16_t* pb = reinterpret_cast<uint16_t*>(tile + sw64_off(row, i + h2));
-        const float x1 = bf16_bits_to_f32(*pa), x2 = bf16_bits_to_f32(*pb);
-        *pa = f32_to_bf16_bits(fmaf(x1, c[e].x, -x2 * c[e].y));
-        *pb = f32_to_bf16_bits(fmaf(x2, c[e].x, x1 * c[e].y));
-      }
-    }
-  }
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
+               "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -203,15 +207,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     ld_pending[k] = true;
   };
-  // wait for buffer k's tiles, then rotate the query rows (pairs split between the halves)
-  auto land_and_rotate = [&](int k, int blk, unsigned int site) -> bool {
+  // wait for buffer k's tiles (the query rows arrive rotated)
+  auto land = [&](int k, unsigned int site) -> bool {
     wait_phase(bar_ld(k), ph_ld[k], abort_flag, lim, site);
     __syncthreads();
     if (*abort_flag) return false;
     ph_ld[k] ^= 1;
     if (tid == 0) ld_pending[k] = false;
-    const long long q = static_cast<long long>(blk) * kRows + row;
-    if (p.r > 0 && q < p.S) bwd_rotate_row(Qb(k), row, q, p.cs, p.r, half);
     return true;
   };
 
@@ -232,8 +234,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ok = false;
   } else {
     if (tid == 0) kv_pending = false;
-    if (p.r > 0 && key < p.S) bwd_rotate_row(Kt, row, key, p.cs, p.r, half);
-    ok = land_and_rotate(0, j, 43);
+    ok = land(0, 43);
   }
   fence_proxy_async_smem();
   tc_fence_before_sync();
@@ -266,7 +267,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after_sync();
 
     // ---- P = exp(S/sqrt(D) - lse), dS = P (dP - delta) / sqrt(D) for this thread's 64
-    //      keys of the row, to shared memory as bf16
+    //      keys of the row, to shared memory as bf16 (once this thread's previous dq'
+    //      reduction has read its staging area there; the barrier below covers the others)
+    bulk_wait_read_all();
+    __syncthreads();
     for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
       uint32_t sr[32], dr[32];
       tmem_ld32(tS + lane_off + c0, sr);
@@ -312,8 +316,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_commit(bar_mma);
       mma_pending = true;
     }
-    // the next block's tiles land and rotate while these MMAs run
-    if (NB == 2 && next && !land_and_rotate(bi ^ 1, i + 1, 44)) { ok = false; break; }
+    // the next block's tiles land while these MMAs run
+    if (NB == 2 && next && !land(bi ^ 1, 44)) { ok = false; break; }
     wait_phase(bar_mma, ph_mma, abort_flag, lim, 41);
     __syncthreads();
     if (*abort_flag) { ok = false; break; }
@@ -321,24 +325,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) mma_pending = false;
     tc_fence_after_sync();
 
-    // ---- this thread's half of the dq' row into the fp32 accumulator
-    float* dq = p.dq_acc + ((static_cast<long long>(b) * p.S + (qvalid ? q : 0)) * p.H + h) * D;
-    for (int c0 = DH * half; c0 < DH * half + DH; c0 += 16) {
+    // ---- this thread's half of the dq' row into the fp32 accumulator: staged in the
+    //      P/dS tiles (free until the next block's P/dS), added by one bulk reduction
+    //      that runs on while the next block proceeds
+    float* stage = reinterpret_cast<float*>(Pt) + (row * 2 + half) * DH;
+    for (int c0 = 0; c0 < DH; c0 += 16) {
       uint32_t r[16];
-      tmem_ld16(tdQ + lane_off + c0, r);
+      tmem_ld16(tdQ + lane_off + DH * half + c0, r);
       tmem_wait_ld();
-      if (qvalid) {
 #pragma unroll
-        for (int k = 0; k < 16; k += 4)
-          red_add_v4(dq + c0 + k, __uint_as_float(r[k]), __uint_as_float(r[k + 1]), __uint_as_float(r[k + 2]),
-                     __uint_as_float(r[k + 3]));
-      }
+      for (int k = 0; k < 16; k += 4)
+        *reinterpret_cast<float4*>(stage + c0 + k) = make_float4(__uint_as_float(r[k]), __uint_as_float(r[k + 1]),
+                                                                 __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
+    }
+    if (qvalid) {
+      fence_proxy_async_smem();
+      bulk_reduce_add_f32(p.dq_acc + ((static_cast<long long>(b) * p.S + q) * p.H + h) * D + DH * half,
+                          smem_u32(stage), DH * 4);
     }
     if (NB == 1 && next) {  // single buffer: the next block's tiles only now
       fence_proxy_async_smem();
       __syncthreads();
       if (tid == 0) issue_qg(0, i + 1);
-      if (!land_and_rotate(0, i + 1, 45)) { ok = false; break; }
+      if (!land(0, 45)) { ok = false; break; }
     }
     fence_proxy_async_smem();
     tc_fence_before_sync();
@@ -346,6 +355,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   // ---- dk = R(key)^T dk' and dv for the rows of key block j, bf16 into slots 1 and 2
+  bulk_wait_read_all();
+  __syncthreads();
   if (ok && !*abort_flag) {
     tc_fence_after_sync();
     const bool kvalid = key < p.S;
@@ -398,7 +409,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
 
-  // ---- teardown: let the copies and MMAs in flight land, then free TMEM
+  // ---- teardown: let the copies, reductions and MMAs in flight land, then free TMEM
+  bulk_wait_all();
   if (tid == 0) {
     if (kv_pending) drain_phase(bar_kv, 0, lim);
     for (int k = 0; k < 2; ++k)

@@ -399,7 +399,7 @@ int encode_rows_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int 
 template <int D>
 int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tg, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.S * p.H;
-  neox::attn_bwd_delta_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
+  neox::attn_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   const int smem = neox::bwd_smem_bytes(D);
@@ -526,14 +526,17 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
       rc = get_table(device, S, rotary_dim, rotary_base, stream, &cs);
       if (rc != NEOX_OK) return rc;
     }
-    // scratch: the fp32 dq' accumulator [B,S,H,D], then delta [B,H,S]
+    // scratch: the fp32 dq' accumulator [B,S,H,D], delta [B,H,S], then (256-byte aligned)
+    // the rotated copy of qkv [B,S,H,3,D] bf16
     const size_t rows = static_cast<size_t>(B) * S * H;
+    const size_t rot_off = (rows * D * sizeof(float) + rows * sizeof(float) + 255) / 256 * 256;
     float* scratch = nullptr;
     int* counters = nullptr;
-    rc = get_scratch(device, rows * D * sizeof(float) + rows * sizeof(float), 1, &scratch, &counters);
+    rc = get_scratch(device, rot_off + rows * 3 * D * 2, 1, &scratch, &counters);
     if (rc != NEOX_OK) return rc;
+    uint16_t* qkv_rot = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(scratch) + rot_off);
     CUtensorMap tq, tg;
-    rc = encode_qkv_map(&tq, qkv, B, S, H, D);
+    rc = encode_qkv_map(&tq, qkv_rot, B, S, H, D);
     if (rc != NEOX_OK) return rc;
     rc = encode_rows_map(&tg, dout, B, S, H, D);
     if (rc != NEOX_OK) return rc;
@@ -543,6 +546,7 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.lse = lse;
     p.dout = static_cast<const uint16_t*>(dout);
     p.dqkv = static_cast<uint16_t*>(dqkv);
+    p.qkv_rot = qkv_rot;
     p.dq_acc = scratch;
     p.delta = scratch + rows * D;
     p.cs = cs;
