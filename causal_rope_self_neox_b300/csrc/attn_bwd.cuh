@@ -133,6 +133,14 @@ __host__ __device__ constexpr int bwd_smem_bytes(int D) {
 }
 constexpr int kBwdThreads = 256;  // two threads per tile row (each half of the columns)
 
+__device__ __forceinline__ uint64_t bwd_fmul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float bwd_lo(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x)); }
+__device__ __forceinline__ float bwd_hi(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x >> 32)); }
+
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
                "r"(bytes)
@@ -277,19 +285,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32(tdP + lane_off + c0, dr);
       tmem_wait_ld();
       uint32_t pk[16], dk[16];
+      // dS = P (dP - delta) / sqrt(D) = P * (dP / sqrt(D) - delta / sqrt(D)), in fp32 pairs
+      const uint64_t sc2 = f32x2_pack(p.scale_log2, p.scale_log2), nl2 = f32x2_pack(-lse2, -lse2);
+      const uint64_t ds2 = f32x2_pack(p.scale, p.scale), nd2 = f32x2_pack(-dl * p.scale, -dl * p.scale);
+      const bool full = qvalid && static_cast<long long>(j) * kRows + c0 + 31 <= q;  // no key past the row
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
-        float pe[2], de[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const long long kk = static_cast<long long>(j) * kRows + c0 + e + u;
-          const bool use = qvalid && kk <= q;
-          const float pv = use ? ex2_approx(fmaf(__uint_as_float(sr[e + u]), p.scale_log2, -lse2)) : 0.0f;
-          pe[u] = pv;
-          de[u] = pv * (__uint_as_float(dr[e + u]) - dl) * p.scale;
+        const uint64_t t = ffma2(f32x2_pack(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sc2, nl2);
+        float p0 = ex2_approx(bwd_lo(t)), p1 = ex2_approx(bwd_hi(t));
+        if (!full) {
+          const long long kk = static_cast<long long>(j) * kRows + c0 + e;
+          if (!(qvalid && kk <= q)) p0 = 0.0f;
+          if (!(qvalid && kk + 1 <= q)) p1 = 0.0f;
         }
-        pk[e / 2] = pack_bf16x2(pe[0], pe[1]);
-        dk[e / 2] = pack_bf16x2(de[0], de[1]);
+        const uint64_t pp = f32x2_pack(p0, p1);
+        const uint64_t d2 = bwd_fmul2(pp, ffma2(f32x2_pack(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), ds2, nd2));
+        pk[e / 2] = pack_bf16x2(p0, p1);
+        dk[e / 2] = pack_bf16x2(bwd_lo(d2), bwd_hi(d2));
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
