@@ -10,8 +10,8 @@
 //   dq'_i = sum_j ds_ij k'_j / sqrt(D)         dk'_j = sum_i ds_ij q'_i / sqrt(D)
 //   dq_i = R(i)^T dq'_i,  dk_j = R(j)^T dk'_j  (the rotation back by -theta).
 // Three kernels on the caller's stream:
-//   attn_bwd_prep_kernel   the rotated q', k' (bf16, rounded once) with v into a scratch
-//                          copy of qkv, delta_i (fp32) and a zeroed fp32 dq' accumulator;
+//   attn_bwd_prep_kernel   the rotated q', k' (bf16, rounded once) into a scratch copy of
+//                          qkv, delta_i (fp32) and a zeroed fp32 dq' accumulator;
 //   attn_bwd_kernel        one CTA per (key block j, head): K'_j, V_j stay in shared
 //                          memory while query blocks i >= j stream through; per block
 //                          five tcgen05 MMAs (S = Q'K'^T and dP = dO V^T into TMEM, then
@@ -34,7 +34,7 @@ struct BwdParams {
   const float* lse;      // fp32 [B, H, S]     (the forward's, natural log)
   const uint16_t* dout;  // bf16 [B, S, H, D]
   uint16_t* dqkv;        // bf16 [B, S, H, 3, D]
-  uint16_t* qkv_rot;     // bf16 [B, S, H, 3, D]  scratch: rotated q', k' and v
+  uint16_t* qkv_rot;     // bf16 [B, S, H, 3, D]  scratch: rotated q', k' in slots 0, 1 (slot 2 unused)
   float* dq_acc;         // fp32 [B, S, H, D]  scratch: dq' before the rotation back
   float* delta;          // fp32 [B, H, S]     scratch
   const float2* cs;      // cos/sin table [>= S rows][r/2]
@@ -46,7 +46,7 @@ struct BwdParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Per row (one warp per row): qkv_rot = (R(s) q, R(s) k, v) in bf16 (the rotation
+// Per row (one warp per row): slots 0, 1 of qkv_rot = R(s) q, R(s) k in bf16 (the rotation
 // rounded once, as the MMAs take it), delta = dout . out (fp32), and dq_acc zeroed.
 // Lane l handles dims l, l + 32, ...; a rotated dim reads its pair partner directly.
 template <int D>
@@ -71,7 +71,6 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
     }
     dst[d] = f32_to_bf16_bits(yq);
     dst[D + d] = f32_to_bf16_bits(yk);
-    dst[2 * D + d] = src[2 * D + d];
   }
   const uint16_t* o = p.out + row * D;
   const uint16_t* g = p.dout + row * D;
@@ -87,33 +86,27 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   }
 }
 
-// dq = R(s)^T dq' (bf16) into slot 0 of dqkv, one thread per row:
-//   dq_i = dq'_i c + dq'_{i+h} s,  dq_{i+h} = dq'_{i+h} c - dq'_i s  (i < h = r/2).
+// dq = R(s)^T dq' (bf16) into slot 0 of dqkv, one warp per row (lane l: dims l, l + 32,
+// ...):  dq_i = dq'_i c + dq'_{i+h} s,  dq_{i+h} = dq'_{i+h} c - dq'_i s  (i < h = r/2).
 template <int D>
-__global__ void __launch_bounds__(128) attn_bwd_dq_kernel(const BwdParams p) {
-  const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;  // [b][s][h]
+__global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // [b][s][h]
+  const int lane = threadIdx.x & 31;
   if (row >= static_cast<long long>(p.B) * p.S * p.H) return;
   const long long s = (row / p.H) % p.S;
   const float* src = p.dq_acc + row * D;
   const int h2 = p.r >> 1;
-  uint4* dst = reinterpret_cast<uint4*>(p.dqkv + row * 3 * D);
-  for (int d0 = 0; d0 < D; d0 += 8) {
-    float y[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int d = d0 + e;
-      float v = src[d];
-      if (d < h2) {
-        const float2 c = p.cs[s * h2 + d];
-        v = fmaf(v, c.x, src[d + h2] * c.y);
-      } else if (d < p.r) {
-        const float2 c = p.cs[s * h2 + (d - h2)];
-        v = fmaf(v, c.x, -src[d - h2] * c.y);
-      }
-      y[e] = v;
+  uint16_t* dst = p.dqkv + row * 3 * D;
+  for (int d = lane; d < D; d += 32) {
+    float v = src[d];
+    if (d < h2) {
+      const float2 c = p.cs[s * h2 + d];
+      v = fmaf(v, c.x, src[d + h2] * c.y);
+    } else if (d < p.r) {
+      const float2 c = p.cs[s * h2 + (d - h2)];
+      v = fmaf(v, c.x, -src[d - h2] * c.y);
     }
-    dst[d0 / 8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                             pack_bf16x2(y[6], y[7]));
+    dst[d] = f32_to_bf16_bits(v);
   }
 }
 
@@ -128,8 +121,15 @@ __host__ __device__ constexpr uint32_t idesc_bwd(int M, int N, bool a_mn, bool b
 __host__ __device__ constexpr int bwd_qbufs(int D) { return D == 128 ? 1 : 2; }
 // smem: K'_j, V_j, then per buffer Q'_i and dO_i, then P_i and dS_i [128][128] tiles
 // (1 KB aligned), barriers, the TMEM address and the abort flag.
+// dq' staging for the bulk reductions: per thread D/2 floats plus 16 bytes of padding, so
+// that the slots of 8 consecutive rows start in 8 different 16-byte bank groups; it
+// reuses the P/dS tiles and, for D = 128, runs 4 KB past them.
+__host__ __device__ constexpr int bwd_stage_slot(int D) { return D / 2 * 4 + 16; }
+__host__ __device__ constexpr int bwd_stage_extra(int D) {
+  return 256 * bwd_stage_slot(D) > 2 * tile_bytes(128) ? 256 * bwd_stage_slot(D) - 2 * tile_bytes(128) : 0;
+}
 __host__ __device__ constexpr int bwd_smem_bytes(int D) {
-  return 1024 + (2 + 2 * bwd_qbufs(D)) * tile_bytes(D) + 2 * tile_bytes(128) + 128;
+  return 1024 + (2 + 2 * bwd_qbufs(D)) * tile_bytes(D) + 2 * tile_bytes(128) + bwd_stage_extra(D) + 128;
 }
 constexpr int kBwdThreads = 256;  // two threads per tile row (each half of the columns)
 
@@ -152,8 +152,8 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg,
-                    const BwdParams p) {
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
+                    const __grid_constant__ CUtensorMap tg, const BwdParams p) {
   constexpr int NB = bwd_qbufs(D);
   constexpr int TB = tile_bytes(D);
   constexpr int DH = D / 2;  // output columns per thread
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto Gb = [&](int k) { return Vt + TB + (2 * k + 1) * TB; };
   uint8_t* Pt = Vt + TB + 2 * NB * TB;
   uint8_t* St = Pt + tile_bytes(128);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(St + tile_bytes(128));  // kv, ld[2], mma
+  uint64_t* bars = reinterpret_cast<uint64_t*>(St + tile_bytes(128) + bwd_stage_extra(D));  // kv, ld[2], mma
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     fence_barrier_init();
     tma_prefetch_map(&tq);
     tma_prefetch_map(&tg);
+    tma_prefetch_map(&tv);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_arrive_expect_tx(bar_kv, 2 * TB);
     for (int cb = 0; cb < D / kBlkCols; ++cb) {
       tma_load_4d(smem_u32(Kt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * h + 1, j * kRows, b);
-      tma_load_4d(smem_u32(Vt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * h + 2, j * kRows, b);
+      tma_load_4d(smem_u32(Vt + cb * kBlkBytes), &tv, bar_kv, cb * kBlkCols, 3 * h + 2, j * kRows, b);
     }
     kv_pending = true;
     issue_qg(0, j);
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ---- this thread's half of the dq' row into the fp32 accumulator: staged in the
     //      P/dS tiles (free until the next block's P/dS), added by one bulk reduction
     //      that runs on while the next block proceeds
-    float* stage = reinterpret_cast<float*>(Pt) + (row * 2 + half) * DH;
+    float* stage = reinterpret_cast<float*>(Pt + (half * kRows + row) * bwd_stage_slot(D));
     for (int c0 = 0; c0 < DH; c0 += 16) {
       uint32_t r[16];
       tmem_ld16(tdQ + lane_off + DH * half + c0, r);

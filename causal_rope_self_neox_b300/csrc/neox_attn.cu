@@ -397,7 +397,8 @@ int encode_rows_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int 
 }
 
 template <int D>
-int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tg, cudaStream_t stream) {
+int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tg,
+               cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.S * p.H;
   neox::attn_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -406,9 +407,9 @@ int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMa
   e = cudaFuncSetAttribute(neox::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   const long long ctas = static_cast<long long>(p.nblk) * p.B * p.H;
-  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tg, p);
+  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tv, tg, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 127) / 128), 128, 0, stream>>>(p);
+  neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   e = cudaGetLastError();
   return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
 }
@@ -535,8 +536,10 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     rc = get_scratch(device, rot_off + rows * 3 * D * 2, 1, &scratch, &counters);
     if (rc != NEOX_OK) return rc;
     uint16_t* qkv_rot = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(scratch) + rot_off);
-    CUtensorMap tq, tg;
+    CUtensorMap tq, tv, tg;  // rotated q', k'; v from the input; dout
     rc = encode_qkv_map(&tq, qkv_rot, B, S, H, D);
+    if (rc != NEOX_OK) return rc;
+    rc = encode_qkv_map(&tv, qkv, B, S, H, D);
     if (rc != NEOX_OK) return rc;
     rc = encode_rows_map(&tg, dout, B, S, H, D);
     if (rc != NEOX_OK) return rc;
@@ -559,9 +562,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
     switch (D) {
-      case 64: return launch_bwd<64>(p, tq, tg, stream);
-      case 96: return launch_bwd<96>(p, tq, tg, stream);
-      default: return launch_bwd<128>(p, tq, tg, stream);
+      case 64: return launch_bwd<64>(p, tq, tv, tg, stream);
+      case 96: return launch_bwd<96>(p, tq, tv, tg, stream);
+      default: return launch_bwd<128>(p, tq, tv, tg, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
