@@ -24,6 +24,9 @@ host cores on a bounded sample of the same workload per step; rank 0 only.
 new token per sequence against a resident K/V cache), in GB/s of cache read per step,
 against the measured HBM copy bandwidth (1 GPU).
 One JSON line on stdout (rank 0); everything else goes to stderr.
+
+--pass bwd times the backward (neox_attn_bwd) on a prefill workload instead: 5 B H S^2 D
+algorithmic FLOPs per step in TFLOP/s, the forward's out/lse and a seeded dout resident.
 """
 from __future__ import annotations
 
