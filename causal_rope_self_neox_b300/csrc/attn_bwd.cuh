@@ -46,40 +46,67 @@ struct BwdParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Per row (one warp per row): slots 0, 1 of qkv_rot = R(s) q, R(s) k in bf16 (the rotation
-// rounded once, as the MMAs take it), delta = dout . out (fp32), and dq_acc zeroed.
-// Lane l handles dims l, l + 32, ...; a rotated dim reads its pair partner directly.
+// Per row (one warp per row): slots 0, 1 of qkv_rot = R(s) q, R(s) k in bf16 (the
+// rotation rounded once, as the MMAs take it), delta = dout . out (fp32), and dq_acc
+// zeroed.  16-byte loads and stores; the row's q and k wait in shared memory (fp32) so
+// that a rotated dim can read its pair partner.
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // [b][s][h]
-  const int lane = threadIdx.x & 31;
+  constexpr int C8 = D / 8;  // 16-byte chunks per D-vector
+  __shared__ float xbuf[8][2 * D];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + w;  // [b][s][h]
   if (row >= static_cast<long long>(p.B) * p.S * p.H) return;
   const long long s = (row / p.H) % p.S;
   const int h2 = p.r >> 1;
+  float* x = xbuf[w];
   const uint16_t* src = p.qkv + row * 3 * D;
   uint16_t* dst = p.qkv_rot + row * 3 * D;
-  for (int d = lane; d < D; d += 32) {
-    float yq = bf16_bits_to_f32(src[d]), yk = bf16_bits_to_f32(src[D + d]);
-    if (d < p.r) {
-      const int i = d < h2 ? d : d - h2;
-      const int partner = d < h2 ? d + h2 : d - h2;
-      const float sg = d < h2 ? -1.0f : 1.0f;  // y_i = x_i c - x_{i+h} s,  y_{i+h} = x_{i+h} c + x_i s
-      const float2 c = p.cs[s * h2 + i];
-      const float pq = bf16_bits_to_f32(src[partner]), pk = bf16_bits_to_f32(src[D + partner]);
-      yq = fmaf(yq, c.x, sg * pq * c.y);
-      yk = fmaf(yk, c.x, sg * pk * c.y);
+  for (int c = lane; c < 2 * C8; c += 32) {  // q chunks then k chunks
+    const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * c);
+    const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[8 * c + 2 * k] = __uint_as_float(wd[k] << 16);
+      x[8 * c + 2 * k + 1] = __uint_as_float(wd[k] & 0xFFFF0000u);
     }
-    dst[d] = f32_to_bf16_bits(yq);
-    dst[D + d] = f32_to_bf16_bits(yk);
+  }
+  __syncwarp();
+  for (int c = lane; c < 2 * C8; c += 32) {
+    const int base = c < C8 ? 0 : D;  // this chunk's vector (q or k) in x
+    float y[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int d = 8 * c + e - base;
+      float v = x[base + d];
+      if (d < p.r) {  // y_i = x_i c - x_{i+h} s,  y_{i+h} = x_{i+h} c + x_i s
+        const bool first = d < h2;
+        const int i = first ? d : d - h2;
+        const float2 cs = p.cs[s * h2 + i];
+        const float partner = x[base + (first ? d + h2 : d - h2)];
+        v = fmaf(v, cs.x, (first ? -partner : partner) * cs.y);
+      }
+      y[e] = v;
+    }
+    *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                        pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
   }
   const uint16_t* o = p.out + row * D;
   const uint16_t* g = p.dout + row * D;
   float acc = 0.0f;
-  for (int d = lane; d < D; d += 32) acc = fmaf(bf16_bits_to_f32(o[d]), bf16_bits_to_f32(g[d]), acc);
+  for (int c = lane; c < C8; c += 32) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + 8 * c), gg = *reinterpret_cast<const uint4*>(g + 8 * c);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wg[4] = {gg.x, gg.y, gg.z, gg.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc = fmaf(__uint_as_float(wa[k] << 16), __uint_as_float(wg[k] << 16), acc);
+      acc = fmaf(__uint_as_float(wa[k] & 0xFFFF0000u), __uint_as_float(wg[k] & 0xFFFF0000u), acc);
+    }
+  }
 #pragma unroll
   for (int k = 16; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
-  float* dq = p.dq_acc + row * D;
-  for (int d = lane; d < D; d += 32) dq[d] = 0.0f;
+  float4* dq = reinterpret_cast<float4*>(p.dq_acc + row * D);
+  for (int c = lane; c < D / 4; c += 32) dq[c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (lane == 0) {
     const long long h = row % p.H, b = row / (static_cast<long long>(p.H) * p.S);
     p.delta[(b * p.H + h) * p.S + s] = acc;
