@@ -39,6 +39,7 @@ struct BwdParams {
   float* delta;          // fp32 [B, H, S]     scratch
   const float2* cs;      // cos/sin table [>= S rows][r/2]
   int B, S, H, r, nblk;
+  int heads_per_group;   // CTA order: groups of heads whose Q'/dO tiles fit in L2 together
   float scale_log2;      // log2(e) / sqrt(D)
   float scale;           // 1 / sqrt(D)
   uint64_t wait_limit_ns;
@@ -198,9 +199,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & (kRows - 1), half = tid >> 7;
+  // CTA order: heads in groups of heads_per_group (their Q'/dO tiles, read by every key
+  // block of a head, stay in L2 while the group runs); inside a group the heaviest key
+  // blocks (j = 0, every query block) come first
   const int BH = p.B * p.H;
-  const int j = blockIdx.x / BH;  // key block; the heaviest (j = 0) blocks are launched first
-  const int bh = blockIdx.x - j * BH;
+  const int per_group = p.heads_per_group * p.nblk;
+  const int grp_id = blockIdx.x / per_group;
+  const int g0 = grp_id * p.heads_per_group;
+  const int gh = min(p.heads_per_group, BH - g0);  // heads in this group (the last may be short)
+  const int rem = blockIdx.x - grp_id * per_group;
+  const int j = rem / gh;
+  const int bh = g0 + (rem - j * gh);
   const int b = bh / p.H, h = bh - b * p.H;
   const uint32_t bar_kv = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[3]);
   auto bar_ld = [&](int k) { return smem_u32(&bars[1 + k]); };

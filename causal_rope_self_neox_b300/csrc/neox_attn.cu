@@ -558,6 +558,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.H = H;
     p.r = rotary_dim;
     p.nblk = static_cast<int>(nblk);
+    // about 48 MB of Q and dO per group of heads (half of L2), at least one head
+    p.heads_per_group = static_cast<int>(std::max<long long>(
+        1, std::min<long long>(static_cast<long long>(B) * H, (48ll << 20) / (static_cast<long long>(S) * D * 4))));
     p.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D)));
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
