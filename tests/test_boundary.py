@@ -122,3 +122,27 @@ def test_decode_invalid_arguments_rejected_before_cuda(lib, args, status):
 
 def test_decode_status_string(lib):
     assert "position" in na.neox_attn_status_string(na.NEOX_ERR_DEVICE_BAD_POSITION)
+
+
+# ---- backward: neox_attn_bwd(qkv, out, lse, dout, B, S, H, D, r, base, dqkv)
+GD = 0x70000000
+DQ = 0x80000000
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, OUT, LSE, GD, 2, 256, 4, 64, 16, 1e4, DQ), na.NEOX_ERR_INVALID_ARG),        # null qkv
+    ((A, 0, LSE, GD, 2, 256, 4, 64, 16, 1e4, DQ), na.NEOX_ERR_INVALID_ARG),          # null out
+    ((A, OUT, 0, GD, 2, 256, 4, 64, 16, 1e4, DQ), na.NEOX_ERR_INVALID_ARG),          # null lse
+    ((A, OUT, LSE, 0, 2, 256, 4, 64, 16, 1e4, DQ), na.NEOX_ERR_INVALID_ARG),         # null dout
+    ((A, OUT, LSE, GD, 2, 256, 4, 64, 16, 1e4, 0), na.NEOX_ERR_INVALID_ARG),         # null dqkv
+    ((A, OUT, LSE, GD, 0, 256, 4, 64, 16, 1e4, DQ), na.NEOX_ERR_INVALID_ARG),        # B = 0
+    ((A, OUT, LSE, GD, 2, 256, 4, 80, 16, 1e4, DQ), na.NEOX_ERR_UNSUPPORTED_HEAD_DIM),
+    ((A, OUT, LSE, GD, 2, 256, 4, 64, 15, 1e4, DQ), na.NEOX_ERR_INVALID_ARG),        # odd rotary_dim
+    ((A, OUT, LSE, GD, 2, 256, 4, 64, 16, 0.0, DQ), na.NEOX_ERR_INVALID_ARG),        # base <= 0
+    ((A, OUT, LSE, GD + 8, 2, 256, 4, 64, 16, 1e4, DQ), na.NEOX_ERR_MISALIGNED),     # dout 8-B aligned
+    ((A, OUT, LSE, GD, 2, 256, 4, 64, 16, 1e4, DQ + 4), na.NEOX_ERR_MISALIGNED),     # dqkv 4-B aligned
+    ((A, OUT, LSE, GD, 2, 256, 4, 64, 16, 1e4, A + 4096), na.NEOX_ERR_INVALID_ARG),  # dqkv overlaps qkv
+    ((A, OUT, LSE, GD, 2, 256, 4, 64, 16, 1e4, GD), na.NEOX_ERR_INVALID_ARG),        # dqkv on dout
+])
+def test_bwd_invalid_arguments_rejected_before_cuda(lib, args, status):
+    assert na.neox_attn_bwd(*args, stream=0) == status
