@@ -114,8 +114,11 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   }
 }
 
-// dq = R(s)^T dq' (bf16) into slot 0 of dqkv, one warp per row (lane l: dims l, l + 32,
-// ...):  dq_i = dq'_i c + dq'_{i+h} s,  dq_{i+h} = dq'_{i+h} c - dq'_i s  (i < h = r/2).
+// dq = R(s)^T dq' (bf16) into slot 0 of dqkv, one warp per row:
+//   dq_i = dq'_i c + dq'_{i+h} s,  dq_{i+h} = dq'_{i+h} c - dq'_i s  (i < h = r/2).
+// When r/2 is a multiple of 4 no 4-dim chunk straddles i = h or i = r, and lane l handles
+// chunk l with 16-byte loads (the partner chunk too) and an 8-byte store; otherwise lane
+// l handles dims l, l + 32, ...
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p) {
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // [b][s][h]
@@ -125,6 +128,23 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p) {
   const float* src = p.dq_acc + row * D;
   const int h2 = p.r >> 1;
   uint16_t* dst = p.dqkv + row * 3 * D;
+  if ((h2 & 3) == 0) {
+    for (int c = lane; c < D / 4; c += 32) {
+      const int d = 4 * c;
+      float4 v = *reinterpret_cast<const float4*>(src + d);
+      if (d < p.r) {
+        const bool first = d < h2;
+        const float4 w = *reinterpret_cast<const float4*>(src + (first ? d + h2 : d - h2));
+        const float sg = first ? 1.0f : -1.0f;
+        const float2* cs = p.cs + s * h2 + (first ? d : d - h2);
+        const float2 c0 = cs[0], c1 = cs[1], c2 = cs[2], c3 = cs[3];
+        v = make_float4(fmaf(v.x, c0.x, sg * w.x * c0.y), fmaf(v.y, c1.x, sg * w.y * c1.y),
+                        fmaf(v.z, c2.x, sg * w.z * c2.y), fmaf(v.w, c3.x, sg * w.w * c3.y));
+      }
+      *reinterpret_cast<uint2*>(dst + d) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    }
+    return;
+  }
   for (int d = lane; d < D; d += 32) {
     float v = src[d];
     if (d < h2) {
