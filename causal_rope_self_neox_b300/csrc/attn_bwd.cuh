@@ -164,7 +164,7 @@ __host__ __device__ constexpr uint32_t idesc_bwd(int M, int N, bool a_mn, bool b
 }
 
 // Query-side buffers (Q'_i and dO_i tile pairs): two for D <= 96, so the next block's
-// tiles load (TMA) and rotate while the current block's MMAs run; one for D = 128, where
+// tiles load (TMA) while the current block's MMAs run; one for D = 128, where
 // a second pair does not fit next to K', V, P and dS.
 __host__ __device__ constexpr int bwd_qbufs(int D) { return D == 128 ? 1 : 2; }
 // smem: K'_j, V_j, then per buffer Q'_i and dO_i, then P_i and dS_i [128][128] tiles

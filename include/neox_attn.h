@@ -182,8 +182,9 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
  * Arithmetic: rotated q', k', the probabilities and ds enter the tensor cores as bf16,
  * everything accumulates in fp32.  Ownership and errors as for neox_attn_fwd.  The
  * library's per-device scratch (shared with neox_attn_decode, grown on demand, freed by
- * neox_attn_release) holds an fp32 dq' accumulator of B*S*H*D and B*H*S floats, so
- * backward and decode calls must not overlap on the GPU.
+ * neox_attn_release) holds an fp32 dq' accumulator of B*S*H*D floats, B*H*S floats of
+ * dout.out, and a bf16 copy of qkv's shape holding the rotated q', k' (about 10 bytes
+ * per element of out in all), so backward and decode calls must not overlap on the GPU.
  */
 int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void* dout, int B, int S, int H, int D,
                   int rotary_dim, float rotary_base, void* dqkv, void* stream);
