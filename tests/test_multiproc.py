@@ -60,6 +60,27 @@ def _head_shards(rank, world, port, result):
     dist.destroy_process_group()
 
 
+def _bwd_head_shards(rank, world, port, result):
+    # the backward is per head too: each rank's head range, gathered, is the whole gradient
+    _init(rank, world, port)
+    import oracle
+    from causal_rope_self_neox_b300.workloads import bf16_bits, make_qkv
+    B, S, H, D, r = 1, 64, 4, 64, 16
+    qkv = make_qkv(B, S, H, D, seed=78)
+    dout = torch.randn((B, S, H, D), generator=torch.Generator().manual_seed(79)).to(torch.bfloat16)
+    per = H // world
+    h0, h1 = rank * per, (rank + 1) * per
+    g = oracle.bwd(bf16_bits(qkv[:, :, h0:h1].contiguous()), bf16_bits(dout[:, :, h0:h1].contiguous()),
+                   B, S, per, D, r, threads=1)
+    parts = [torch.empty((B, S, per, 3, D), dtype=torch.float64) for _ in range(world)]
+    dist.all_gather(parts, torch.from_numpy(g))
+    if rank == 0:
+        full = oracle.bwd(bf16_bits(qkv), bf16_bits(dout), B, S, H, D, r, threads=1)
+        result["equal"] = bool(np.array_equal(torch.cat(parts, dim=2).numpy(), full))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
 def _timing(rank, world, port, result):
     _init(rank, world, port)
     import bench
@@ -82,6 +103,10 @@ def _spawn(fn):
 
 def test_head_shards_gather_to_the_full_result():
     assert _spawn(_head_shards)["equal"]
+
+
+def test_backward_head_shards_gather_to_the_full_gradient():
+    assert _spawn(_bwd_head_shards)["equal"]
 
 
 def test_benchmark_timing_is_max_over_ranks():
