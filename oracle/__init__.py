@@ -57,6 +57,10 @@ def _load():
             lib.neox_oracle_decode.restype = i32
             lib.neox_oracle_bwd.argtypes = [P, P, i32, i32, i32, i32, i32, f64, P, i32]
             lib.neox_oracle_bwd.restype = i32
+            lib.neox_oracle_alibi_slopes.argtypes = [i32, P]
+            lib.neox_oracle_alibi_slopes.restype = None
+            lib.neox_oracle_fwd_alibi.argtypes = [P, i32, i32, i32, i32, P, P, i32]
+            lib.neox_oracle_fwd_alibi.restype = i32
             _lib = lib
     return _lib
 
@@ -173,3 +177,23 @@ def bwd(qkv_bits: np.ndarray, dout_bits: np.ndarray, B: int, S: int, H: int, D: 
     if rc != 0:
         raise ValueError(f"oracle backward failed ({rc})")
     return dqkv
+
+
+def alibi_slopes(H: int) -> np.ndarray:
+    """The ALiBi slope of each of H heads (fp64)."""
+    out = np.zeros(H, dtype=np.float64)
+    _load().neox_oracle_alibi_slopes(H, _ptr(out))
+    return out
+
+
+def fwd_alibi(qkv_bits: np.ndarray, B: int, S: int, H: int, D: int, threads: int | None = None):
+    """Causal attention with the ALiBi bias -m_h (i - j) and no rotation.
+
+    qkv_bits: bf16 bits [B,S,H,3,D].  Returns (out fp64 [B,S,H,D], lse fp64 [B,H,S])."""
+    q = _u16(qkv_bits, (B, S, H, 3, D))
+    out = np.zeros((B, S, H, D), dtype=np.float64)
+    lse = np.zeros((B, H, S), dtype=np.float64)
+    rc = _load().neox_oracle_fwd_alibi(_ptr(q), B, S, H, D, _ptr(out), _ptr(lse), threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle ALiBi forward failed ({rc})")
+    return out, lse

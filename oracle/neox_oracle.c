@@ -578,3 +578,110 @@ int neox_oracle_bwd(const uint16_t* qkv, const uint16_t* dout, int B, int S, int
   pthread_mutex_destroy(&J.mu);
   return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
+
+/* ------------------------------------------------------------------ ALiBi ----
+ * The pages name ALiBi ("linear bias attention") as GPT-NeoX's other positional scheme
+ * ("gpt-neox - 模型与框架" page, section "位置编码"; GPT-NeoX library summary, "Key
+ * capabilities") but print no formula.  Reading: the scheme as published with the
+ * method (Press et al., "Train Short, Test Long"): no rotation; head h adds
+ * -m_h * (i - j) to the score of query i and key j <= i; the slopes form a geometric
+ * sequence 2^(-8/n), 2^(-16/n), ... for a power-of-two head count n, and for other head
+ * counts the slopes of the largest power of two n below H are followed by every other
+ * slope of 2n (the odd-numbered ones), until H slopes are reached.                  */
+void neox_oracle_alibi_slopes(int H, double* slopes) {
+  int n = 1;
+  while (n * 2 <= H) n *= 2;
+  for (int k = 0; k < n && k < H; ++k) slopes[k] = pow(2.0, -8.0 * (double)(k + 1) / (double)n);
+  for (int k = n, e = 1; k < H; ++k, e += 2) slopes[k] = pow(2.0, -8.0 * (double)e / (double)(2 * n));
+}
+
+typedef struct {
+  const uint16_t* qkv;
+  int B, S, H, D;
+  const double* slopes;
+  double* out;
+  double* lse;
+  pthread_mutex_t mu;
+  int64_t next, n_items;
+  int failed;
+} ajob_t;
+
+static void* worker_alibi(void* arg) {
+  ajob_t* J = (ajob_t*)arg;
+  const int S = J->S, H = J->H, D = J->D;
+  const double inv_sqrt_d = 1.0 / sqrt((double)D);
+  double* sc = malloc(sizeof(double) * (size_t)S);
+  double* q = malloc(sizeof(double) * (size_t)D);
+  if (!sc || !q) {
+    pthread_mutex_lock(&J->mu);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->mu);
+  } else {
+    for (;;) {
+      pthread_mutex_lock(&J->mu);
+      int64_t item = J->next < J->n_items ? J->next++ : -1;
+      pthread_mutex_unlock(&J->mu);
+      if (item < 0) break;
+      /* item = (b, h, i): one query row */
+      const int64_t i = item % S, bh = item / S, h = bh % H, b = bh / H;
+      const double m_h = J->slopes[h];
+      const uint16_t* qs = J->qkv + qkv_off(b, i, h, 0, S, H, D);
+      for (int d = 0; d < D; ++d) q[d] = bf16_to_f64(qs[d]);
+      double mx = -INFINITY;
+      for (int64_t j = 0; j <= i; ++j) {
+        const uint16_t* kj = J->qkv + qkv_off(b, j, h, 1, S, H, D);
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += q[d] * bf16_to_f64(kj[d]);
+        sc[j] = dot * inv_sqrt_d - m_h * (double)(i - j);
+        if (sc[j] > mx) mx = sc[j];
+      }
+      double l = 0.0;
+      for (int64_t j = 0; j <= i; ++j) {
+        sc[j] = exp(sc[j] - mx);
+        l += sc[j];
+      }
+      double* o = J->out + ((b * S + i) * H + h) * (int64_t)D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (int64_t j = 0; j <= i; ++j) {
+        const uint16_t* vj = J->qkv + qkv_off(b, j, h, 2, S, H, D);
+        for (int d = 0; d < D; ++d) o[d] += sc[j] / l * bf16_to_f64(vj[d]);
+      }
+      J->lse[(b * H + h) * (int64_t)S + i] = mx + log(l);
+    }
+  }
+  free(sc);
+  free(q);
+  return NULL;
+}
+
+/* Causal attention with the ALiBi bias instead of the rotation.
+ * qkv: bf16 bits [B,S,H,3,D]; out fp64 [B,S,H,D]; lse fp64 [B,H,S] (natural log). */
+int neox_oracle_fwd_alibi(const uint16_t* qkv, int B, int S, int H, int D, double* out, double* lse, int threads) {
+  if (!qkv || !out || !lse || B < 1 || S < 1 || H < 1 || D < 1) return ORACLE_ERR_ARG;
+  double* slopes = malloc(sizeof(double) * (size_t)H);
+  if (!slopes) return ORACLE_ERR_NOMEM;
+  neox_oracle_alibi_slopes(H, slopes);
+  ajob_t J;
+  memset(&J, 0, sizeof J);
+  J.qkv = qkv;
+  J.B = B;
+  J.S = S;
+  J.H = H;
+  J.D = D;
+  J.slopes = slopes;
+  J.out = out;
+  J.lse = lse;
+  J.n_items = (int64_t)B * H * S;
+  pthread_mutex_init(&J.mu, NULL);
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pthread_t tid[256];
+  int started = 0;
+  for (int t = 0; t < threads; ++t)
+    if (pthread_create(&tid[t], NULL, worker_alibi, &J) == 0) ++started;
+  if (started == 0) worker_alibi(&J);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&J.mu);
+  free(slopes);
+  return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
