@@ -254,6 +254,50 @@ def run_reference(args, w):
     return 0
 
 
+def run_reference_bwd(args, w):
+    """The backward oracle as the reference arm of the backward line: each step is a
+    bounded sample of whole heads of batch 0, timed on the host cores."""
+    import oracle
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import torch
+    threads = oracle.default_threads()
+    qkv = make_qkv(w.B, w.S, w.H, w.D, w.seed, w.k_scale)
+    dout = torch.randn((w.B, w.S, w.H, w.D), generator=torch.Generator().manual_seed(w.seed + 7)).to(torch.bfloat16)
+    head_flops = 5.0 * w.S * w.S * w.D
+    t0 = time.perf_counter()  # calibrate: one head on one thread
+    oracle.bwd(bf16_bits(qkv[:1, :, :1].contiguous()), bf16_bits(dout[:1, :, :1].contiguous()), 1, w.S, 1, w.D,
+               w.rotary_dim, w.rotary_base, threads=1)
+    per_head_1t = time.perf_counter() - t0
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    heads = int(max(1, min(w.H, per_step_budget / per_head_1t * threads)))
+    q1 = bf16_bits(qkv[:1, :, :heads].contiguous())
+    g1 = bf16_bits(dout[:1, :, :heads].contiguous())
+    used = min(threads, heads)
+    for _ in range(args.warmup):
+        oracle.bwd(q1, g1, 1, w.S, heads, w.D, w.rotary_dim, w.rotary_base, threads=used)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.bwd(q1, g1, 1, w.S, heads, w.D, w.rotary_dim, w.rotary_base, threads=used)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = heads * head_flops * args.steps / total / 1e12
+    line = {
+        "metric": BWD_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "pass": "backward", "sample_heads_per_step": heads, "l2": "n/a (CPU)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+                         "sample": f"{heads} of {w.B * w.H} heads x {w.S} rows per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------- rank timing ----
 def max_over_ranks(x: float, dist, device) -> float:
     """The slowest rank's value (a timing); the identity with no process group."""
@@ -667,8 +711,7 @@ def main():
     w = WORKLOADS[args.workload]
     if args.pass_ == "bwd":
         if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the backward line has no reference arm"}))
-            return 0
+            return run_reference_bwd(args, w)
         return run_bwd(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
