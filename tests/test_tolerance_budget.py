@@ -162,3 +162,23 @@ def test_bwd_rounding_points_fit_tolerances_with_margin(B, S, H, D, r):
         rel = np.sqrt((e ** 2).mean()) / np.sqrt((ref[..., slot, :] ** 2).mean())
         mrel = np.abs(e).max() / np.abs(ref[..., slot, :]).max()
         assert mrel <= BWD_MAX_REL / 2 and rel <= BWD_REL_RMS / 2, (slot, mrel, rel)
+
+
+# ------------------------------------------------------------------- decode ----
+# The decode kernel never reads the angle of key 128 t + row from the table directly for
+# rotary_dim <= 32: it multiplies the fp32 table entries (cos, sin)(128 t w) and
+# (cos, sin)(row w) (angle addition).  The product must stay far below bf16's 2^-9.
+@pytest.mark.parametrize("r", [8, 16, 24, 32])
+def test_decode_angle_addition_error(r):
+    base, h = 10000.0, r // 2
+    w = base ** (-2.0 * np.arange(h) / r)
+    f32 = lambda x: np.asarray(x, dtype=np.float32).astype(np.float64)
+    worst = 0.0
+    for t in (0, 1, 7, 15, 63, 127):  # tiles up to position 16383
+        for row in (0, 1, 37, 127):
+            a, b = 128 * t * w, row * w
+            ct, st, cr, sr = f32(np.cos(a)), f32(np.sin(a)), f32(np.cos(b)), f32(np.sin(b))
+            c = f32(f32(ct * cr) - f32(st * sr))
+            s = f32(f32(st * cr) + f32(ct * sr))
+            worst = max(worst, np.abs(c - np.cos(a + b)).max(), np.abs(s - np.sin(a + b)).max())
+    assert worst < 1e-6, worst  # 2^-9 = 2.0e-3
