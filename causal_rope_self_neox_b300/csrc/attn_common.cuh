@@ -83,6 +83,33 @@ __device__ __forceinline__ bool wait_phase_inline(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same bounded wait with the CTA's abort flag given as a 32-bit shared-memory address
+// (fewer live registers than a generic pointer in the register-heavy roles).
+__device__ __forceinline__ int flag_ld(uint32_t a) {
+  int v;
+  asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void flag_st(uint32_t a, int v) {
+  asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ bool wait_phase_s(uint32_t bar, uint32_t parity, uint32_t abort_addr, uint64_t limit_ns,
+                                             unsigned int site) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (flag_ld(abort_addr)) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      flag_st(abort_addr, 1);
+      record_error(kErrTimeout, site);
+      return false;
+    }
+  }
+}
+
 // Drain wait used on the abort path: waits for an in-flight async operation to land,
 // ignoring the abort flag, still bounded.
 __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, uint64_t limit_ns) {

@@ -62,31 +62,22 @@ __host__ __device__ constexpr int rot_kind(int r) {
 // float4 table entries per row loaded ahead of a tile's data.
 __host__ __device__ constexpr int rot_ahead(int rk) { return rk == kRotR16 ? 4 : rk == kRotR24 ? 6 : rk == kRotR32 ? 8 : 0; }
 
+// Shared-memory carve-up, identical on host and device: the two query tiles (each followed
+// by its side tile), the K ring (each slot a tile and its side tile), the V ring, then the
+// barrier block.  Offsets are closed forms of the slot index (no arrays, so no local memory).
 struct WsLayout {
-  int q_raw[2], q_side[2];
-  int k_raw[kMaxRing], k_side[kMaxRing];
-  int v[kMaxRing];
-  int bars;
-  int total;
+  int tb, sb;    // bytes of a D-column tile and of a side tile
+  int nk, nv;
+  __host__ __device__ int q_raw(int t) const { return t * (tb + sb); }
+  __host__ __device__ int q_side(int t) const { return t * (tb + sb) + tb; }
+  __host__ __device__ int k_raw(int s) const { return (2 + s) * (tb + sb); }
+  __host__ __device__ int k_side(int s) const { return (2 + s) * (tb + sb) + tb; }
+  __host__ __device__ int v(int s) const { return (2 + nk) * (tb + sb) + s * tb; }
+  __host__ __device__ int bars() const { return (2 + nk) * (tb + sb) + nv * tb; }
+  __host__ __device__ int total() const { return bars() + 64 * 8 + 16 + 1024; }  // + TMEM slot, flag, alignment slack
 };
-
-// Shared-memory carve-up; identical on host and device.
 __host__ __device__ inline WsLayout ws_layout(int D, int side_cols, int NK, int NV) {
-  WsLayout L{};
-  int off = 0;
-  for (int t = 0; t < 2; ++t) {
-    L.q_raw[t] = off; off += tile_bytes(D);
-    L.q_side[t] = off; off += tile_bytes(side_cols);
-  }
-  for (int s = 0; s < NK; ++s) {
-    L.k_raw[s] = off; off += tile_bytes(D);
-    L.k_side[s] = off; off += tile_bytes(side_cols);
-  }
-  for (int s = 0; s < NV; ++s) { L.v[s] = off; off += tile_bytes(D); }
-  L.bars = off;
-  off += 64 * 8 + 16;  // barriers, TMEM slot, abort flag
-  L.total = off + 1024;  // + alignment slack
-  return L;
+  return WsLayout{tile_bytes(D), tile_bytes(side_cols), NK, NV};
 }
 
 // Barrier indices inside the barrier block.
@@ -139,10 +130,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NK = p.nk, NV = p.nv;
   const WsLayout L = ws_layout(D, p.side_cols, NK, NV);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 64);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  // barrier block: 64 mbarriers, then the TMEM address slot and the abort flag (32-bit
+  // shared addresses throughout)
+  const uint32_t bar0 = smem_u32(smem) + static_cast<uint32_t>(L.bars());
+  const uint32_t tmem_slot_a = bar0 + 64 * 8, abort_a = tmem_slot_a + 4;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint64_t lim = p.wait_limit_ns;
@@ -168,27 +160,27 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       mbar_init(bar(BAR_V_FULL + s), 1);
       mbar_init(bar(BAR_V_EMPTY + s), 1);
     }
-    *abort_flag = 0;
+    flag_st(abort_a, 0);
     fence_barrier_init();
     tma_prefetch_map(&tmap);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(tmem_slot_a, 512);
     tmem_relinquish();
   }
   // side tiles start at zero; columns >= r are never written again
   if (RK != kRotNone) {
     const int sb = tile_bytes(p.side_cols);
     for (int i = tid * 16; i < sb; i += kWsThreads * 16) {
-      for (int t = 0; t < 2; ++t) *reinterpret_cast<uint4*>(smem + L.q_side[t] + i) = make_uint4(0, 0, 0, 0);
-      for (int s = 0; s < NK; ++s) *reinterpret_cast<uint4*>(smem + L.k_side[s] + i) = make_uint4(0, 0, 0, 0);
+      for (int t = 0; t < 2; ++t) *reinterpret_cast<uint4*>(smem + L.q_side(t) + i) = make_uint4(0, 0, 0, 0);
+      for (int s = 0; s < NK; ++s) *reinterpret_cast<uint4*>(smem + L.k_side(s) + i) = make_uint4(0, 0, 0, 0);
     }
   }
   fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = static_cast<uint32_t>(flag_ld(tmem_slot_a));
   // register split: the softmax warpgroups hold a whole 128-column S row per thread
   // (launch: 384 x 168 = 128 x 136 + 256 x 184)
 
@@ -211,44 +203,44 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const int k = snake_unit(rd, blockIdx.x, G);
         if (k >= p.num_units) continue;
         const Unit u = decode_unit(k, p.B, p.H, p.S);
-        if (!wait_phase(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_flag, lim, 10)) { ok = false; break; }
+        if (!wait_phase_s(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_a, lim, 10)) { ok = false; break; }
         const int nq = u.n1 > 0 ? 2 : 1;
         mbar_arrive_expect_tx(bar(BAR_Q_FULL), tile_bytes(D) * nq);
         last_q_par = u_local & 1;
         for (int t = 0; t < nq; ++t)
           for (int cb = 0; cb < D / kBlkCols; ++cb)
-            tma_load_4d_hint(smem_u32(smem + L.q_raw[t] + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
+            tma_load_4d_hint(smem_u32(smem + L.q_raw(t) + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
                              3 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
         // K_j before V_{j-1}: the order in which the MMA warp consumes them
         for (int j = 0; j <= u.nkv && ok; ++j) {
           if (j < u.nkv) {
             const int s = ks;
             const uint32_t par = kph;
-            if (!wait_phase(bar(BAR_K_EMPTY + s), par ^ 1, abort_flag, lim, 11)) { ok = false; break; }
+            if (!wait_phase_s(bar(BAR_K_EMPTY + s), par ^ 1, abort_a, lim, 11)) { ok = false; break; }
             mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D));
             k_armed |= 1u << s;
             k_par = (k_par & ~(1u << s)) | (par << s);
             for (int cb = 0; cb < D / kBlkCols; ++cb)
-              tma_load_4d_hint(smem_u32(smem + L.k_raw[s] + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s),
+              tma_load_4d_hint(smem_u32(smem + L.k_raw(s) + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s),
                                cb * kBlkCols, 3 * u.h + 1, j * kRows, u.b, pol_kv);
             if (++ks == NK) { ks = 0; kph ^= 1; }
           }
           if (j >= 1) {
             const int s = vs;
             const uint32_t par = vph;
-            if (!wait_phase(bar(BAR_V_EMPTY + s), par ^ 1, abort_flag, lim, 12)) { ok = false; break; }
+            if (!wait_phase_s(bar(BAR_V_EMPTY + s), par ^ 1, abort_a, lim, 12)) { ok = false; break; }
             mbar_arrive_expect_tx(bar(BAR_V_FULL + s), tile_bytes(D));
             v_armed |= 1u << s;
             v_par = (v_par & ~(1u << s)) | (par << s);
             for (int cb = 0; cb < D / kBlkCols; ++cb)
-              tma_load_4d_hint(smem_u32(smem + L.v[s] + cb * kBlkBytes), &tmap, bar(BAR_V_FULL + s), cb * kBlkCols,
+              tma_load_4d_hint(smem_u32(smem + L.v(s) + cb * kBlkBytes), &tmap, bar(BAR_V_FULL + s), cb * kBlkCols,
                                3 * u.h + 2, (j - 1) * kRows, u.b, pol_kv);
             if (++vs == NV) { vs = 0; vph ^= 1; }
           }
         }
         ++u_local;
       }
-      if (!ok || *abort_flag) {
+      if (!ok || flag_ld(abort_a)) {
         // let every load this thread armed land before the CTA's shared memory goes away
         if (last_q_par >= 0) drain_phase(bar(BAR_Q_FULL), last_q_par, lim);
         for (int s = 0; s < NK; ++s)
@@ -270,19 +262,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       // Every operand buffer sits at a fixed shared address for the whole kernel, so each
       // descriptor is a base below plus a constant: the issue loop is adds and MMAs only.
-      const uint64_t dq[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_raw[0]))),
-                              desc_of(desc_lo_k(smem_u32(smem + L.q_raw[1])))};
+      const uint64_t dq[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_raw(0)))),
+                              desc_of(desc_lo_k(smem_u32(smem + L.q_raw(1))))};
       // query descriptors of every 16-column chunk, both tiles (fixed for the kernel)
       uint64_t qd[2][D / 16];
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int kc = 0; kc < D / 16; ++kc) qd[t][kc] = dq[t] + kchunk_off(kc);
-      const uint64_t dqs[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_side[0]))),
-                               desc_of(desc_lo_k(smem_u32(smem + L.q_side[1])))};
-      const uint64_t dk0 = desc_of(desc_lo_k(smem_u32(smem + L.k_raw[0])));
-      const uint64_t dks0 = desc_of(desc_lo_k(smem_u32(smem + L.k_side[0])));
-      const uint64_t dv0 = desc_of(desc_lo_v(smem_u32(smem + L.v[0])));
+      const uint64_t dqs[2] = {desc_of(desc_lo_k(smem_u32(smem + L.q_side(0)))),
+                               desc_of(desc_lo_k(smem_u32(smem + L.q_side(1))))};
+      const uint64_t dk0 = desc_of(desc_lo_k(smem_u32(smem + L.k_raw(0))));
+      const uint64_t dks0 = desc_of(desc_lo_k(smem_u32(smem + L.k_side(0))));
+      const uint64_t dv0 = desc_of(desc_lo_v(smem_u32(smem + L.v(0))));
       const uint32_t kstep = static_cast<uint32_t>(tile_bytes(D) + tile_bytes(p.side_cols)) >> 4;
       const uint32_t vstep = static_cast<uint32_t>(tile_bytes(D)) >> 4;
       int kslot = 0, vslot = 0;
@@ -292,7 +284,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       const int nside = p.r16 / 16;  // 16-column chunks of lo products (<= 8)
       bool ok = true, issued = false;
       auto wait_all = [&](int b, uint32_t par, unsigned int site) {
-        return __all_sync(0xffffffffu, wait_phase(bar(b), par, abort_flag, lim, site));
+        return __all_sync(0xffffffffu, wait_phase_s(bar(b), par, abort_a, lim, site));
       };
       for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
         const int k = snake_unit(rd, blockIdx.x, G);
@@ -364,7 +356,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         ++u_local;
       }
-      if (issued && __any_sync(0xffffffffu, !ok || *abort_flag)) {
+      if (issued && __any_sync(0xffffffffu, !ok || flag_ld(abort_a))) {
         tc_commit_l(lead, bar(BAR_DRAIN));
         drain_phase(bar(BAR_DRAIN), 0, lim);
       }
@@ -404,13 +396,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const bool isq = it < nq;
         const int s = kslot;
         const int blk = isq ? 2 * u.t + it : it - nq;  // 128-row block of the sequence
-        if (isq ? (it == 0 && !wait_phase(bar(BAR_Q_FULL), u_local & 1, abort_flag, lim, 20))
-                : !wait_phase(bar(BAR_K_FULL + s), kph, abort_flag, lim, 21)) {
+        if (isq ? (it == 0 && !wait_phase_s(bar(BAR_Q_FULL), u_local & 1, abort_a, lim, 20))
+                : !wait_phase_s(bar(BAR_K_FULL + s), kph, abort_a, lim, 21)) {
           ok = false;
           break;
         }
-        uint8_t* tile = smem + (isq ? L.q_raw[it] : L.k_raw[s]);
-        uint8_t* side = smem + (isq ? L.q_side[it] : L.k_side[s]);
+        uint8_t* tile = smem + (isq ? L.q_raw(it) : L.k_raw(s));
+        uint8_t* side = smem + (isq ? L.q_side(it) : L.k_side(s));
         if (RK == kRotR24) {  // packed cross terms of dims 16..23 (see the MMA issue)
           rotate_row_small<3>(tile, side, tt, ta0, isq ? 1 : 2);
           rotate_row_small<3>(tile, side, tt + 64, ta1, isq ? 1 : 2);
@@ -467,34 +459,41 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       bool ok = true;
 #pragma unroll 1
       for (int j = 0; j < n; ++j) {
-        if (!__all_sync(0xffffffffu, wait_phase_inline(bar(BAR_S_FULL + tau), s_use & 1, abort_flag, lim, 40))) {
+        if (!__all_sync(0xffffffffu, wait_phase_s(bar(BAR_S_FULL + tau), s_use & 1, abort_a, lim, 40))) {
           ok = false;
           break;
         }
         ++s_use;
         tc_fence_after_sync();
         uint32_t sr[128];
+        float mx;
+        if (j != qt) {
+          // below the diagonal: the loads return each 32-column chunk's max as well
+          float mq[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
-        tmem_wait_ld();
-        // causal mask on the diagonal block: keys > row get -inf (the block's keys are
-        // 128*qt + c, its rows 128*qt + row)
-        if (j == qt) {
+          for (int c = 0; c < 4; ++c) mq[c] = tmem_ld32_max(tS + c * 32, sr + c * 32);
+          tmem_wait_ld();
+          mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
+          tmem_wait_ld();
+          // the diagonal block: keys > row get -inf (the block's keys are 128*qt + c, its
+          // rows 128*qt + row), then the row max in eight chains of 3-input max
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > row) sr[c] = __float_as_uint(-INFINITY);
-        }
-        // row max: eight independent chains of 3-input max over 16 columns each
-        float mc[8];
+          float mc[8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const uint32_t* v = sr + 16 * g;
-          float m = fmax3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t* v = sr + 16 * g;
+            float m = fmax3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
 #pragma unroll
-          for (int q = 3; q < 15; q += 2) m = fmax3f(m, __uint_as_float(v[q]), __uint_as_float(v[q + 1]));
-          mc[g] = fmaxf(m, __uint_as_float(v[15]));
+            for (int q = 3; q < 15; q += 2) m = fmax3f(m, __uint_as_float(v[q]), __uint_as_float(v[q + 1]));
+            mc[g] = fmaxf(m, __uint_as_float(v[15]));
+          }
+          mx = fmaxf(fmax3f(mc[0], mc[1], mc[2]), fmax3f(fmax3f(mc[3], mc[4], mc[5]), mc[6], mc[7]));
         }
-        const float mx = fmaxf(fmax3f(mc[0], mc[1], mc[2]), fmax3f(fmax3f(mc[3], mc[4], mc[5]), mc[6], mc[7]));
         const float mx_s = mx * sl2;
         float m_new = m_used;
         bool rescale = false;
@@ -544,7 +543,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         mbar_arrive(bar(BAR_P_FULL + tau));
       }
       if (!ok) break;
-      if (!__all_sync(0xffffffffu, wait_phase_inline(bar(BAR_O_FINAL + tau), o_use & 1, abort_flag, lim, 41))) break;
+      if (!__all_sync(0xffffffffu, wait_phase_s(bar(BAR_O_FINAL + tau), o_use & 1, abort_a, lim, 41))) break;
       ++o_use;
       tc_fence_after_sync();
       const int qrow = qt * kRows + row;
@@ -588,7 +587,7 @@ inline void pick_rings(int D, int side_cols, int* nk, int* nv) {
   const int pref_k = D == 64 ? 4 : D == 96 ? 3 : 2, pref_v = D == 64 ? 4 : 2;
   const int cand[][2] = {{pref_k, pref_v}, {3, 2}, {2, 2}, {2, 1}, {1, 1}};
   for (const auto& c : cand) {
-    if (ws_layout(D, side_cols, c[0], c[1]).total <= kSmemLimit) {
+    if (ws_layout(D, side_cols, c[0], c[1]).total() <= kSmemLimit) {
       *nk = c[0];
       *nv = c[1];
       return;
@@ -602,12 +601,12 @@ int launch_ws_impl(const CUtensorMap& map, AttnParams p, int num_sms, cudaStream
   pick_rings(D, p.side_cols, &p.nk, &p.nv);
   const WsLayout L = ws_layout(D, p.side_cols, p.nk, p.nv);
   auto kern = attn_fwd_ws_kernel<D, RK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total());
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   const int T = (p.S + 255) / 256;
   p.num_units = p.B * p.H * T;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-  kern<<<grid, kWsThreads, L.total, stream>>>(map, p);
+  kern<<<grid, kWsThreads, L.total(), stream>>>(map, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   return 0;
