@@ -8,7 +8,11 @@
 //   warp 0        TMA producer: Q tiles once per unit, then K_j / V_j into rings
 //   warp 1        tcgen05 issuer (one lane) and TMEM owner
 //   warps 2-3     rotary transform: rotate-half of Q (per unit) and of K_j (per block)
-//                 in shared memory, hi in place, lo to the side tiles
+//                 in shared memory, hi in place, lo to the side tiles.  A unit's K_0 is
+//                 loaded and rotated before its query tiles: K_0's ring slot frees a few
+//                 blocks before the previous unit releases the query buffers, so only the
+//                 query load and rotation remain between two units (the producer also
+//                 prefetches the next unit's query tiles into L2)
 //   warps 4-7     softmax + lazy correction + epilogue of query tile 0
 //   warps 8-11    the same for query tile 1
 //
@@ -199,10 +203,26 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       uint32_t k_armed = 0, k_par = 0, v_armed = 0, v_par = 0;
       int last_q_par = -1;
       bool ok = true;
+      auto load_k = [&](const Unit& u, int j) {
+        const int s = ks;
+        const uint32_t par = kph;
+        if (!wait_phase_s(bar(BAR_K_EMPTY + s), par ^ 1, abort_a, lim, 11)) return false;
+        mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D));
+        k_armed |= 1u << s;
+        k_par = (k_par & ~(1u << s)) | (par << s);
+        for (int cb = 0; cb < D / kBlkCols; ++cb)
+          tma_load_4d_hint(smem_u32(smem + L.k_raw(s) + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s), cb * kBlkCols,
+                           3 * u.h + 1, j * kRows, u.b, pol_kv);
+        if (++ks == NK) { ks = 0; kph ^= 1; }
+        return true;
+      };
       for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
         const int k = snake_unit(rd, blockIdx.x, G);
         if (k >= p.num_units) continue;
         const Unit u = decode_unit(k, p.B, p.H, p.S);
+        // K_0 first: its ring slot frees a few blocks before the previous unit's last S
+        // MMA releases the query buffers, so it is loaded (and rotated) off the boundary
+        if (!load_k(u, 0)) { ok = false; break; }
         if (!wait_phase_s(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_a, lim, 10)) { ok = false; break; }
         const int nq = u.n1 > 0 ? 2 : 1;
         mbar_arrive_expect_tx(bar(BAR_Q_FULL), tile_bytes(D) * nq);
@@ -211,21 +231,20 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           for (int cb = 0; cb < D / kBlkCols; ++cb)
             tma_load_4d_hint(smem_u32(smem + L.q_raw(t) + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
                              3 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
-        // K_j before V_{j-1}: the order in which the MMA warp consumes them
-        for (int j = 0; j <= u.nkv && ok; ++j) {
-          if (j < u.nkv) {
-            const int s = ks;
-            const uint32_t par = kph;
-            if (!wait_phase_s(bar(BAR_K_EMPTY + s), par ^ 1, abort_a, lim, 11)) { ok = false; break; }
-            mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D));
-            k_armed |= 1u << s;
-            k_par = (k_par & ~(1u << s)) | (par << s);
-            for (int cb = 0; cb < D / kBlkCols; ++cb)
-              tma_load_4d_hint(smem_u32(smem + L.k_raw(s) + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s),
-                               cb * kBlkCols, 3 * u.h + 1, j * kRows, u.b, pol_kv);
-            if (++ks == NK) { ks = 0; kph ^= 1; }
+        // the next unit's query tiles into L2 now, so their load at the next boundary is short
+        {
+          const int kn = snake_unit(rd + 1, blockIdx.x, G);
+          if (kn < p.num_units) {
+            const Unit un = decode_unit(kn, p.B, p.H, p.S);
+            for (int t = 0; t < (un.n1 > 0 ? 2 : 1); ++t)
+              for (int cb = 0; cb < D / kBlkCols; ++cb)
+                tma_prefetch_l2_4d(&tmap, cb * kBlkCols, 3 * un.h + 0, (2 * un.t + t) * kRows, un.b);
           }
-          if (j >= 1) {
+        }
+        // K_j before V_{j-1}: the order in which the MMA warp consumes them
+        for (int j = 1; j <= u.nkv && ok; ++j) {
+          if (j < u.nkv && !load_k(u, j)) { ok = false; break; }
+          {
             const int s = vs;
             const uint32_t par = vph;
             if (!wait_phase_s(bar(BAR_V_EMPTY + s), par ^ 1, abort_a, lim, 12)) { ok = false; break; }
@@ -364,8 +383,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     }
    } else {
     // ======================================================= rotary transform ====
-    // Per unit the tiles arrive as: query tile 0, query tile 1 (if any), K_0, K_1, ...
-    // One loop over that list, one rotation call site.
+    // Per unit the tiles arrive as: K_0, query tile 0, query tile 1 (if any), K_1, K_2, ...
+    // (the producer's order).  One loop over that list, one rotation call site.
     const int tt = tid - 64;  // 0..63: rows tt and tt + 64 of every tile
     const int h = p.r >> 1;
     constexpr int AH = rot_ahead(RK);
@@ -383,26 +402,27 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     int kslot = 0;
     uint32_t kph = 0, u_local = 0;
     bool ok = true;
-    int rd0 = 0;
-    while (rd0 * G < p.num_units && snake_unit(rd0, blockIdx.x, G) >= p.num_units) ++rd0;
-    if (AH > 0 && rd0 * G < p.num_units) load_ahead(2 * decode_unit(snake_unit(rd0, blockIdx.x, G), p.B, p.H, p.S).t);
-    for (int rd = rd0; rd * G < p.num_units && ok; ++rd) {
+    if (AH > 0) load_ahead(0);  // every unit starts with K_0
+    for (int rd = 0; rd * G < p.num_units && ok; ++rd) {
       const int k = snake_unit(rd, blockIdx.x, G);
       if (k >= p.num_units) continue;
       const Unit u = decode_unit(k, p.B, p.H, p.S);
       const int nq = u.n1 > 0 ? 2 : 1;
+      // item it: 0 -> K_0, 1..nq -> query tile it-1, then K_(it - nq)
+      auto blk_of = [&](int it) { return it == 0 ? 0 : it <= nq ? 2 * u.t + it - 1 : it - nq; };
 #pragma unroll 1
       for (int it = 0; it < nq + u.nkv; ++it) {
-        const bool isq = it < nq;
+        const bool isq = it >= 1 && it <= nq;
+        const int qt = it - 1;  // query tile (when isq)
         const int s = kslot;
-        const int blk = isq ? 2 * u.t + it : it - nq;  // 128-row block of the sequence
-        if (isq ? (it == 0 && !wait_phase_s(bar(BAR_Q_FULL), u_local & 1, abort_a, lim, 20))
+        const int blk = blk_of(it);  // 128-row block of the sequence
+        if (isq ? (qt == 0 && !wait_phase_s(bar(BAR_Q_FULL), u_local & 1, abort_a, lim, 20))
                 : !wait_phase_s(bar(BAR_K_FULL + s), kph, abort_a, lim, 21)) {
           ok = false;
           break;
         }
-        uint8_t* tile = smem + (isq ? L.q_raw(it) : L.k_raw(s));
-        uint8_t* side = smem + (isq ? L.q_side(it) : L.k_side(s));
+        uint8_t* tile = smem + (isq ? L.q_raw(qt) : L.k_raw(s));
+        uint8_t* side = smem + (isq ? L.q_side(qt) : L.k_side(s));
         if (RK == kRotR24) {  // packed cross terms of dims 16..23 (see the MMA issue)
           rotate_row_small<3>(tile, side, tt, ta0, isq ? 1 : 2);
           rotate_row_small<3>(tile, side, tt + 64, ta1, isq ? 1 : 2);
@@ -419,20 +439,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           rotate_row(tile, side, tt + 64, pos_of(blk, tt + 64), p.cs, p.r);
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(isq ? (it == 0 ? BAR_Q_READY : BAR_Q_READY1) : BAR_K_READY + s));
+        mbar_arrive(bar(isq ? (qt == 0 ? BAR_Q_READY : BAR_Q_READY1) : BAR_K_READY + s));
         if (!isq && ++kslot == NK) {
           kslot = 0;
           kph ^= 1;
         }
-        // table entries of the next tile in this list, or of the next unit's query tile 0
-        if (AH > 0) {
-          if (it + 1 < nq + u.nkv) {
-            load_ahead(it + 1 < nq ? 2 * u.t + it + 1 : it + 1 - nq);
-          } else {
-            const int kn = snake_unit(rd + 1, blockIdx.x, G);
-            if (kn < p.num_units) load_ahead(2 * decode_unit(kn, p.B, p.H, p.S).t);
-          }
-        }
+        // table entries of the next tile in this list, or of the next unit's K_0
+        if (AH > 0) load_ahead(it + 1 < nq + u.nkv ? blk_of(it + 1) : 0);
       }
       ++u_local;
     }

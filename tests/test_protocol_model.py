@@ -34,9 +34,14 @@ def roles(units, NK, NV):
         ks = vs = 0
         kuse, vuse = [0] * NK, [0] * NV
         for ul, (n0, n1, nkv) in enumerate(units):
+            # K_0 of the unit first: its slot frees before the previous unit's last S
+            yield ("wait", f"K_EMPTY{ks}", kuse[ks])
+            kuse[ks] += 1
+            yield ("arrive", f"K_FULL{ks}")
+            ks = (ks + 1) % NK
             yield ("wait", "Q_EMPTY", ul)
             yield ("arrive", "Q_FULL")
-            for j in range(nkv + 1):  # K_j before V_{j-1}
+            for j in range(1, nkv + 1):  # K_j before V_{j-1}
                 if j < nkv:
                     yield ("wait", f"K_EMPTY{ks}", kuse[ks])
                     kuse[ks] += 1
@@ -52,11 +57,15 @@ def roles(units, NK, NV):
         ks = 0
         kuse = [0] * NK
         for ul, (n0, n1, nkv) in enumerate(units):
-            yield ("wait", "Q_FULL", ul + 1)
-            yield ("arrive", "Q_READY0")
-            if n1:
-                yield ("arrive", "Q_READY1")
-            for j in range(nkv):
+            # the producer's order: K_0, the query tiles, then K_1 ...
+            items = ["K"] + ["Q"] + ["K"] * (nkv - 1)
+            for item in items:
+                if item == "Q":
+                    yield ("wait", "Q_FULL", ul + 1)
+                    yield ("arrive", "Q_READY0")
+                    if n1:
+                        yield ("arrive", "Q_READY1")
+                    continue
                 kuse[ks] += 1
                 yield ("wait", f"K_FULL{ks}", kuse[ks])
                 yield ("arrive", f"K_READY{ks}")
