@@ -343,11 +343,15 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
 
+    rotation = {"auto": na.NEOX_ROTATION_AUTO, "fused": na.NEOX_ROTATION_FUSED, "pre": na.NEOX_ROTATION_PRE}[args.rotation]
+    # the placement the library takes (the header's documented rule for "auto")
+    pre = args.rotation == "pre" or (args.rotation == "auto" and w.rotary_dim >= 64 and w.rotary_dim % 16 == 0)
+
     def step(q=qkv):
-        rc = na.neox_attn_fwd(q.data_ptr(), w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, out.data_ptr(),
-                              lse.data_ptr(), sh)
+        rc = na.neox_attn_fwd_ex(q.data_ptr(), w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, out.data_ptr(),
+                                 lse.data_ptr(), rotation, sh)
         if rc != 0:
-            raise na.NeoxAttnError(rc, "neox_attn_fwd")
+            raise na.NeoxAttnError(rc, "neox_attn_fwd_ex")
 
     for _ in range(args.warmup):
         flush()
@@ -422,7 +426,7 @@ def run_ours(args, w):
     if rank == 0:
         peak, peak_sus, hbm, src = load_peaks()
         per_gpu = w.flops / (ms_per_step / 1e3) / 1e12
-        traffic, tsrc = profiled_traffic(w.name)
+        traffic, tsrc = profiled_traffic(("pre_" if pre else "") + w.name)
         alg_bytes = 2 * w.B * w.S * w.H * 3 * w.D + 2 * w.B * w.S * w.H * w.D + 4 * w.B * w.H * w.S
         D = w.D
         line = {
@@ -430,6 +434,8 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, K x k_scale)",
             "config": {**w.describe(), "l2": L2_NOTE,
+                       "rotation": f"{args.rotation} -> " + ("pre-rotation pass + attention kernel" if pre
+                                                             else "fused in the attention kernel"),
                        "parallelism": f"replicas x{world} (each rank its own workload; no collective on the data path)"},
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s",
                          "frac": per_gpu / peak, "traffic": traffic,
@@ -446,8 +452,8 @@ def run_ours(args, w):
                     "h2d_bytes_per_step": host_in.numel() * host_in.element_size(),
                     "d2h_bytes_per_step": host_out.numel() * host_out.element_size() + host_lse.numel() * 4,
                     "steps": e2e_steps, "ms_per_step": e2e_ms,
-                    "path": "pinned host qkv -> device, neox_attn_fwd (C ABI), out + lse -> pinned host"},
-            "gpu_launches": args.steps,
+                    "path": "pinned host qkv -> device, neox_attn_fwd_ex (C ABI), out + lse -> pinned host"},
+            "gpu_launches": (2 if pre else 1) * args.steps,
             "wall_s_timed_region": wall,
             "kernel_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
         }
@@ -698,6 +704,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS), default="neox20b")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rotation", choices=["auto", "fused", "pre"], default="auto",
+                    help="where the forward applies the rotary embedding (neox_attn_fwd_ex placement)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
                     help="bwd: time the backward (neox_attn_bwd) on a prefill workload")
     args = ap.parse_args()

@@ -25,7 +25,11 @@ NEOX_ERR_NO_DEVICE_SUPPORT = -6
 NEOX_ERR_TOO_LARGE = -7
 NEOX_ERR_DEVICE_BAD_POSITION = -8
 
-EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
+NEOX_ROTATION_AUTO = 0
+NEOX_ROTATION_FUSED = 1
+NEOX_ROTATION_PRE = 2
+
+EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_ex", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
            "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
            "neox_attn_version", "neox_attn_fwd_noalloc", "neox_attn_decode", "neox_attn_bwd")
 
@@ -52,6 +56,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             for name in ("neox_attn_fwd", "neox_attn_fwd_simple", "neox_attn_fwd_noalloc"):
                 getattr(lib, name).argtypes = fwd_args
                 getattr(lib, name).restype = i32
+            lib.neox_attn_fwd_ex.argtypes = [P, i32, i32, i32, i32, i32, f32, P, P, i32, P]
+            lib.neox_attn_fwd_ex.restype = i32
             lib.neox_attn_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
             lib.neox_attn_decode.restype = i32
             lib.neox_attn_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P]
@@ -78,6 +84,13 @@ def neox_attn_fwd(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int,
                   out_ptr: int, lse_ptr: int, stream: int = 0) -> int:
     """Raw call: device pointers and a cudaStream_t handle as integers; returns a status."""
     return load_library().neox_attn_fwd(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr, stream)
+
+
+def neox_attn_fwd_ex(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
+                     out_ptr: int, lse_ptr: int, rotation: int, stream: int = 0) -> int:
+    """Raw call with the rotation placement (NEOX_ROTATION_AUTO / _FUSED / _PRE)."""
+    return load_library().neox_attn_fwd_ex(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr, rotation,
+                                           stream)
 
 
 def neox_attn_fwd_simple(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
@@ -143,11 +156,13 @@ def neox_attn_version() -> int:
 # ----------------------------------------------------- torch convenience ----
 
 def attn_fwd(qkv, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=None, stream=None,
-             kernel: str = "default"):
+             kernel: str = "default", rotation: int = NEOX_ROTATION_AUTO):
     """Causal NeoX-rotary attention forward on CUDA tensors.
 
     ``qkv``: bf16 ``[B, S, H, 3, D]`` contiguous on a CUDA device.  Returns
     ``(out[B,S,H,D] bf16, lse[B,H,S] fp32)``; ``out``/``lse`` may be passed in.
+    ``rotation`` places the rotary embedding (NEOX_ROTATION_AUTO / _FUSED / _PRE, see
+    ``neox_attn_fwd_ex``); ``kernel="simple"`` runs the plain cross-check kernel.
     torch only allocates memory and supplies the stream; the library computes.
     """
     import torch
@@ -163,10 +178,13 @@ def attn_fwd(qkv, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=N
         lse = torch.empty((B, H, S), dtype=torch.float32, device=qkv.device)
     if stream is None:
         stream = torch.cuda.current_stream(qkv.device)
-    fn = neox_attn_fwd if kernel == "default" else neox_attn_fwd_simple
     with torch.cuda.device(qkv.device):
-        rc = fn(qkv.data_ptr(), B, S, H, D, rotary_dim, float(rotary_base), out.data_ptr(), lse.data_ptr(),
-                stream.cuda_stream)
+        if kernel == "default":
+            rc = neox_attn_fwd_ex(qkv.data_ptr(), B, S, H, D, rotary_dim, float(rotary_base), out.data_ptr(),
+                                  lse.data_ptr(), rotation, stream.cuda_stream)
+        else:
+            rc = neox_attn_fwd_simple(qkv.data_ptr(), B, S, H, D, rotary_dim, float(rotary_base), out.data_ptr(),
+                                      lse.data_ptr(), stream.cuda_stream)
     if rc != NEOX_OK:
         raise NeoxAttnError(rc, "neox_attn_fwd")
     return out, lse

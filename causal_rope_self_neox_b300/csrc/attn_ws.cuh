@@ -127,9 +127,14 @@ __device__ __forceinline__ int snake_unit(int round, int cta, int G) {
   return round * G + ((round & 1) ? (G - 1 - cta) : cta);
 }
 
-template <int D, int RK>
+// PRE: the operands come pre-rotated (rope_prerotate_kernel: hi and lo of q' and k' in
+// the copy that tmap_rot views as [B, S, 4H, D]); the query tiles and K tiles are then
+// loaded with their side tiles by TMA and nothing is rotated here (r % 16 == 0 only).
+template <int D, int RK, bool PRE>
 __global__ void __launch_bounds__(kWsThreads, 1)
-    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const AttnParams p) {
+    attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rot,
+                       const AttnParams p) {
+  static_assert(!PRE || (RK != kRotR24 && RK != kRotScalar), "pre-rotated operands need rotary_dim % 16 == 0");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NK = p.nk, NV = p.nv;
@@ -167,6 +172,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     flag_st(abort_a, 0);
     fence_barrier_init();
     tma_prefetch_map(&tmap);
+    if (PRE) tma_prefetch_map(&tmap_rot);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot_a, 512);
@@ -207,12 +213,21 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const int s = ks;
         const uint32_t par = kph;
         if (!wait_phase_s(bar(BAR_K_EMPTY + s), par ^ 1, abort_a, lim, 11)) return false;
-        mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D));
+        mbar_arrive_expect_tx(bar(BAR_K_FULL + s), tile_bytes(D) + (PRE ? tile_bytes(p.side_cols) : 0));
         k_armed |= 1u << s;
         k_par = (k_par & ~(1u << s)) | (par << s);
-        for (int cb = 0; cb < D / kBlkCols; ++cb)
-          tma_load_4d_hint(smem_u32(smem + L.k_raw(s) + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s), cb * kBlkCols,
-                           3 * u.h + 1, j * kRows, u.b, pol_kv);
+        if (PRE) {  // hi into the tile, lo into its side tile
+          for (int cb = 0; cb < D / kBlkCols; ++cb)
+            tma_load_4d_hint(smem_u32(smem + L.k_raw(s) + cb * kBlkBytes), &tmap_rot, bar(BAR_K_FULL + s),
+                             cb * kBlkCols, 4 * u.h + 2, j * kRows, u.b, pol_kv);
+          for (int cb = 0; cb < p.side_cols / kBlkCols; ++cb)
+            tma_load_4d_hint(smem_u32(smem + L.k_side(s) + cb * kBlkBytes), &tmap_rot, bar(BAR_K_FULL + s),
+                             cb * kBlkCols, 4 * u.h + 3, j * kRows, u.b, pol_kv);
+        } else {
+          for (int cb = 0; cb < D / kBlkCols; ++cb)
+            tma_load_4d_hint(smem_u32(smem + L.k_raw(s) + cb * kBlkBytes), &tmap, bar(BAR_K_FULL + s), cb * kBlkCols,
+                             3 * u.h + 1, j * kRows, u.b, pol_kv);
+        }
         if (++ks == NK) { ks = 0; kph ^= 1; }
         return true;
       };
@@ -225,20 +240,34 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (!load_k(u, 0)) { ok = false; break; }
         if (!wait_phase_s(bar(BAR_Q_EMPTY), (u_local & 1) ^ 1, abort_a, lim, 10)) { ok = false; break; }
         const int nq = u.n1 > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(bar(BAR_Q_FULL), tile_bytes(D) * nq);
+        mbar_arrive_expect_tx(bar(BAR_Q_FULL), (tile_bytes(D) + (PRE ? tile_bytes(p.side_cols) : 0)) * nq);
         last_q_par = u_local & 1;
-        for (int t = 0; t < nq; ++t)
-          for (int cb = 0; cb < D / kBlkCols; ++cb)
-            tma_load_4d_hint(smem_u32(smem + L.q_raw(t) + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
-                             3 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
+        for (int t = 0; t < nq; ++t) {
+          if (PRE) {
+            for (int cb = 0; cb < D / kBlkCols; ++cb)
+              tma_load_4d_hint(smem_u32(smem + L.q_raw(t) + cb * kBlkBytes), &tmap_rot, bar(BAR_Q_FULL),
+                               cb * kBlkCols, 4 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
+            for (int cb = 0; cb < p.side_cols / kBlkCols; ++cb)
+              tma_load_4d_hint(smem_u32(smem + L.q_side(t) + cb * kBlkBytes), &tmap_rot, bar(BAR_Q_FULL),
+                               cb * kBlkCols, 4 * u.h + 1, (2 * u.t + t) * kRows, u.b, pol_q);
+          } else {
+            for (int cb = 0; cb < D / kBlkCols; ++cb)
+              tma_load_4d_hint(smem_u32(smem + L.q_raw(t) + cb * kBlkBytes), &tmap, bar(BAR_Q_FULL), cb * kBlkCols,
+                               3 * u.h + 0, (2 * u.t + t) * kRows, u.b, pol_q);
+          }
+        }
         // the next unit's query tiles into L2 now, so their load at the next boundary is short
         {
           const int kn = snake_unit(rd + 1, blockIdx.x, G);
           if (kn < p.num_units) {
             const Unit un = decode_unit(kn, p.B, p.H, p.S);
             for (int t = 0; t < (un.n1 > 0 ? 2 : 1); ++t)
-              for (int cb = 0; cb < D / kBlkCols; ++cb)
-                tma_prefetch_l2_4d(&tmap, cb * kBlkCols, 3 * un.h + 0, (2 * un.t + t) * kRows, un.b);
+              for (int cb = 0; cb < D / kBlkCols; ++cb) {
+                if (PRE)
+                  tma_prefetch_l2_4d(&tmap_rot, cb * kBlkCols, 4 * un.h + 0, (2 * un.t + t) * kRows, un.b);
+                else
+                  tma_prefetch_l2_4d(&tmap, cb * kBlkCols, 3 * un.h + 0, (2 * un.t + t) * kRows, un.b);
+              }
           }
         }
         // K_j before V_{j-1}: the order in which the MMA warp consumes them
@@ -387,7 +416,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     // (the producer's order).  One loop over that list, one rotation call site.
     const int tt = tid - 64;  // 0..63: rows tt and tt + 64 of every tile
     const int h = p.r >> 1;
-    constexpr int AH = rot_ahead(RK);
+    constexpr int AH = PRE ? 0 : rot_ahead(RK);
     float4 ta0[8], ta1[8];  // table entries of rows tt / tt + 64, loaded one tile ahead
     auto pos_of = [&](int blk, int row) -> int64_t {
       const int64_t pos = static_cast<int64_t>(blk) * kRows + row;
@@ -423,7 +452,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         uint8_t* tile = smem + (isq ? L.q_raw(qt) : L.k_raw(s));
         uint8_t* side = smem + (isq ? L.q_side(qt) : L.k_side(s));
-        if (RK == kRotR24) {  // packed cross terms of dims 16..23 (see the MMA issue)
+        if (PRE) {
+          // operands arrive rotated: only hand them on
+        } else if (RK == kRotR24) {  // packed cross terms of dims 16..23 (see the MMA issue)
           rotate_row_small<3>(tile, side, tt, ta0, isq ? 1 : 2);
           rotate_row_small<3>(tile, side, tt + 64, ta1, isq ? 1 : 2);
         } else if (RK == kRotR16 || RK == kRotR32) {
@@ -609,31 +640,43 @@ inline void pick_rings(int D, int side_cols, int* nk, int* nv) {
   *nk = *nv = 1;
 }
 
-template <int D, int RK>
-int launch_ws_impl(const CUtensorMap& map, AttnParams p, int num_sms, cudaStream_t stream, int* last_err) {
+template <int D, int RK, bool PRE>
+int launch_ws_impl(const CUtensorMap& map, const CUtensorMap& map_rot, AttnParams p, int num_sms, cudaStream_t stream,
+                   int* last_err) {
   pick_rings(D, p.side_cols, &p.nk, &p.nv);
   const WsLayout L = ws_layout(D, p.side_cols, p.nk, p.nv);
-  auto kern = attn_fwd_ws_kernel<D, RK>;
+  auto kern = attn_fwd_ws_kernel<D, RK, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total());
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   const int T = (p.S + 255) / 256;
   p.num_units = p.B * p.H * T;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
-  kern<<<grid, kWsThreads, L.total(), stream>>>(map, p);
+  kern<<<grid, kWsThreads, L.total(), stream>>>(map, map_rot, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   return 0;
 }
 
+// pre_rotated: map_rot views the rotated copy written by rope_prerotate_kernel (the caller
+// checks rotary_dim % 16 == 0 and rotary_dim > 0); otherwise map_rot is not read.
 template <int D>
-int launch_attn_ws(const CUtensorMap& map, const AttnParams& p, int num_sms, cudaStream_t stream, int* last_err) {
+int launch_attn_ws(const CUtensorMap& map, const CUtensorMap& map_rot, bool pre_rotated, const AttnParams& p,
+                   int num_sms, cudaStream_t stream, int* last_err) {
+  if (pre_rotated) {
+    switch (rot_kind(p.r)) {
+      case kRotR16: return launch_ws_impl<D, kRotR16, true>(map, map_rot, p, num_sms, stream, last_err);
+      case kRotR32: return launch_ws_impl<D, kRotR32, true>(map, map_rot, p, num_sms, stream, last_err);
+      case kRotGroups: return launch_ws_impl<D, kRotGroups, true>(map, map_rot, p, num_sms, stream, last_err);
+      default: return -1;
+    }
+  }
   switch (rot_kind(p.r)) {
-    case kRotNone: return launch_ws_impl<D, kRotNone>(map, p, num_sms, stream, last_err);
-    case kRotR16: return launch_ws_impl<D, kRotR16>(map, p, num_sms, stream, last_err);
-    case kRotR24: return launch_ws_impl<D, kRotR24>(map, p, num_sms, stream, last_err);
-    case kRotR32: return launch_ws_impl<D, kRotR32>(map, p, num_sms, stream, last_err);
-    case kRotGroups: return launch_ws_impl<D, kRotGroups>(map, p, num_sms, stream, last_err);
-    default: return launch_ws_impl<D, kRotScalar>(map, p, num_sms, stream, last_err);
+    case kRotNone: return launch_ws_impl<D, kRotNone, false>(map, map_rot, p, num_sms, stream, last_err);
+    case kRotR16: return launch_ws_impl<D, kRotR16, false>(map, map_rot, p, num_sms, stream, last_err);
+    case kRotR24: return launch_ws_impl<D, kRotR24, false>(map, map_rot, p, num_sms, stream, last_err);
+    case kRotR32: return launch_ws_impl<D, kRotR32, false>(map, map_rot, p, num_sms, stream, last_err);
+    case kRotGroups: return launch_ws_impl<D, kRotGroups, false>(map, map_rot, p, num_sms, stream, last_err);
+    default: return launch_ws_impl<D, kRotScalar, false>(map, map_rot, p, num_sms, stream, last_err);
   }
 }
 

@@ -159,6 +159,8 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D
 // ------------------------------------------------------------------ launches ----
 struct Prepared {
   CUtensorMap map;
+  CUtensorMap map_rot;  // the pre-rotated copy (pre == true only)
+  bool pre = false;
   neox::AttnParams p;
   DeviceInfo dev;
   int device;
@@ -207,8 +209,9 @@ int launch_simple(const Prepared& P, cudaStream_t stream) {
 
 template <int D>
 int launch_ws(Prepared& P, cudaStream_t stream) {
-  const int rc = neox::launch_attn_ws<D>(P.map, P.p, P.dev.num_sms, stream, &g_last_cuda_error);
-  return rc == 0 ? NEOX_OK : NEOX_ERR_CUDA;
+  const int rc = neox::launch_attn_ws<D>(P.map, P.pre ? P.map_rot : P.map, P.pre, P.p, P.dev.num_sms, stream,
+                                         &g_last_cuda_error);
+  return rc == 0 ? NEOX_OK : rc == -1 ? NEOX_ERR_INVALID_ARG : NEOX_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------- decode ----
@@ -259,6 +262,46 @@ int get_scratch(int device, size_t bytes, size_t heads, float** out, int** cnt) 
   g_scratch.push_back(Scratch{device, grown, ptr, ncnt, c});
   *out = ptr;
   *cnt = c;
+  return NEOX_OK;
+}
+
+// TMA view of the pre-rotated copy [B, S, H, 4, D] bf16 (slots: q hi, q lo, k hi, k lo)
+// as 4-D {D, 4H, S, B} with the same {32, 1, 128, 1} box and swizzle as the qkv view.
+int encode_rot_map(CUtensorMap* map, const void* rot, int B, int S, int H, int D) {
+  if (!resolve_encode()) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(4) * H, static_cast<cuuint64_t>(S),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(4) * H * D * 2,
+                           static_cast<cuuint64_t>(S) * 4 * H * D * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(neox::kBlkCols), 1, static_cast<cuuint32_t>(neox::kRows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(rot), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return NEOX_OK;
+}
+
+// The separate pre-rotation pass: q' and k' of every row, split hi/lo, into the library's
+// per-device scratch, then the tensor map the attention kernel loads them through.
+template <int D>
+int prerotate(Prepared& P, const void* qkv, cudaStream_t stream) {
+  const neox::AttnParams& p = P.p;
+  const int64_t rows = static_cast<int64_t>(p.B) * p.S * p.H;
+  float* scratch = nullptr;
+  int* counters = nullptr;
+  int rc = get_scratch(P.device, static_cast<size_t>(rows) * 4 * D * 2, 1, &scratch, &counters);
+  if (rc != NEOX_OK) return rc;
+  uint16_t* rot = reinterpret_cast<uint16_t*>(scratch);
+  const int64_t blocks = (rows + 7) / 8;
+  if (blocks > 0x7FFFFFFF) return NEOX_ERR_INVALID_ARG;
+  neox::rope_prerotate_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(qkv), rot, p.cs, rows, p.S, p.H, p.r);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  rc = encode_rot_map(&P.map_rot, rot, p.B, p.S, p.H, D);
+  if (rc != NEOX_OK) return rc;
+  P.pre = true;
   return NEOX_OK;
 }
 
@@ -418,13 +461,26 @@ int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMa
 
 extern "C" {
 
-int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out, float* lse,
-                  void* stream) {
+int neox_attn_fwd_ex(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out,
+                     float* lse, int rotation, void* stream) {
   try {
+    if (rotation != NEOX_ROTATION_AUTO && rotation != NEOX_ROTATION_FUSED && rotation != NEOX_ROTATION_PRE)
+      return NEOX_ERR_INVALID_ARG;
+    const bool pre_ok = rotary_dim > 0 && rotary_dim % 16 == 0;
+    if (rotation == NEOX_ROTATION_PRE && !pre_ok) return NEOX_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Prepared P;
     int rc = prepare(qkv, B, S, H, D, rotary_dim, rotary_base, out, lse, st, &P);
     if (rc != NEOX_OK) return rc;
+    const bool pre = rotation == NEOX_ROTATION_PRE || (rotation == NEOX_ROTATION_AUTO && pre_ok && rotary_dim >= 64);
+    if (pre) {
+      switch (D) {
+        case 64: rc = prerotate<64>(P, qkv, st); break;
+        case 96: rc = prerotate<96>(P, qkv, st); break;
+        default: rc = prerotate<128>(P, qkv, st); break;
+      }
+      if (rc != NEOX_OK) return rc;
+    }
     switch (D) {
       case 64: return launch_ws<64>(P, st);
       case 96: return launch_ws<96>(P, st);
@@ -433,6 +489,11 @@ int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, f
   } catch (...) {
     return NEOX_ERR_CUDA;
   }
+}
+
+int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out, float* lse,
+                  void* stream) {
+  return neox_attn_fwd_ex(qkv, B, S, H, D, rotary_dim, rotary_base, out, lse, NEOX_ROTATION_AUTO, stream);
 }
 
 int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out,

@@ -235,13 +235,11 @@ __device__ __forceinline__ void rotate_row_small(uint8_t* __restrict__ tile, uin
   }
 }
 
-// r % 16 == 0: eight pairs (i0..i0+7 with partners i0+h..i0+h+7) per step, two chunks
-// in, four chunks out.
-__device__ __forceinline__ void rotate_group8(uint8_t* __restrict__ tile, uint8_t* __restrict__ side, int row, int i0,
-                                              int h, const float4* t) {
-  float x[8], z[8], y[8], w[8];
-  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0)), x);
-  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0 + h)), z);
+// Eight pairs (x_i, z_i) turned by the angles in t (four float4 = (cos, sin) of two
+// consecutive pairs each): y = x cos - z sin, w = z cos + x sin, in fp32.  The one place
+// this arithmetic is written, so the in-kernel rotation and the pre-rotation pass give
+// bit-identical results.
+__device__ __forceinline__ void rotate_pairs8(const float* x, const float* z, const float4* t, float* y, float* w) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float cth = (i & 1) ? t[i >> 1].z : t[i >> 1].x;
@@ -249,6 +247,16 @@ __device__ __forceinline__ void rotate_group8(uint8_t* __restrict__ tile, uint8_
     y[i] = fmaf(x[i], cth, -z[i] * sth);
     w[i] = fmaf(z[i], cth, x[i] * sth);
   }
+}
+
+// r % 16 == 0: eight pairs (i0..i0+7 with partners i0+h..i0+h+7) per step, two chunks
+// in, four chunks out.
+__device__ __forceinline__ void rotate_group8(uint8_t* __restrict__ tile, uint8_t* __restrict__ side, int row, int i0,
+                                              int h, const float4* t) {
+  float x[8], z[8], y[8], w[8];
+  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0)), x);
+  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0 + h)), z);
+  rotate_pairs8(x, z, t, y, w);
   uint4 hi, lo;
   split8(y, hi, lo);
   *reinterpret_cast<uint4*>(tile + sw64_off(row, i0)) = hi;
@@ -280,6 +288,49 @@ __device__ __forceinline__ void rotate_two_rows_groups(uint8_t* tile, uint8_t* s
     }
     rotate_group8(tile, side, row0, i0 + 8, h, t0 + 4);
     rotate_group8(tile, side, row1, i0 + 8, h, t1 + 4);
+  }
+}
+
+// Pre-rotation pass (the alternative to rotating K tiles inside the attention kernel for
+// every query unit): writes rot[B, S, H, 4, D] bf16 with slot 0 = hi(q'), 1 = lo(q'),
+// 2 = hi(k'), 3 = lo(k') where q' = R(s) q, k' = R(s) k and lo is zero at dims >= r, so
+// the attention kernel can load the split operands with TMA and rotate nothing.  Needs
+// r % 16 == 0 (the side tiles then hold plain lo columns).  One warp per (b, s, h) row:
+// lanes 0..15 do q, lanes 16..31 do k, lane c of a half owns the 8-dim chunk c; a chunk
+// of the first half of the rotated dims also writes its partner chunk.
+template <int D>
+__global__ void __launch_bounds__(256) rope_prerotate_kernel(const uint16_t* __restrict__ qkv, uint16_t* __restrict__ rot,
+                                                             const float2* __restrict__ cs, int64_t rows, int S, int H,
+                                                             int r) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int which = lane >> 4;  // 0: q, 1: k
+  const int c = lane & 15;      // 8-dim chunk
+  if (c >= D / 8) return;
+  const int h = r >> 1;
+  const int64_t pos = (row / H) % S;  // row = (b * S + s) * H + hd
+  const uint16_t* src = qkv + row * 3 * D + which * D;
+  uint16_t* hi = rot + row * 4 * D + 2 * which * D;
+  uint16_t* lo = hi + D;
+  if (8 * c < h) {
+    const int i0 = 8 * c;
+    float x[8], z[8], y[8], w[8];
+    unpack8(*reinterpret_cast<const uint4*>(src + i0), x);
+    unpack8(*reinterpret_cast<const uint4*>(src + i0 + h), z);
+    float4 t[4];
+    cs_load_n<4>(t, cs, h, i0, pos);
+    rotate_pairs8(x, z, t, y, w);
+    uint4 a, b;
+    split8(y, a, b);
+    *reinterpret_cast<uint4*>(hi + i0) = a;
+    *reinterpret_cast<uint4*>(lo + i0) = b;
+    split8(w, a, b);
+    *reinterpret_cast<uint4*>(hi + i0 + h) = a;
+    *reinterpret_cast<uint4*>(lo + i0 + h) = b;
+  } else if (8 * c >= r) {
+    *reinterpret_cast<uint4*>(hi + 8 * c) = *reinterpret_cast<const uint4*>(src + 8 * c);
+    *reinterpret_cast<uint4*>(lo + 8 * c) = make_uint4(0, 0, 0, 0);
   }
 }
 

@@ -68,7 +68,9 @@ typedef enum {
  * Ownership: the caller owns qkv/out/lse; the library neither frees nor keeps
  * them.  The library owns one cached fp32 cos/sin table per (device, rotary_dim,
  * rotary_base), grown on demand; the call that builds or grows it synchronizes
- * `stream` once, later calls do not.  neox_attn_release() frees the cache.
+ * `stream` once, later calls do not.  neox_attn_release() frees the cache.  When
+ * the rotation is placed in a separate pass (see neox_attn_fwd_ex), the rotated copy
+ * lives in the library's per-device scratch.
  *
  * Errors: every argument is validated before any CUDA call; on error nothing is
  * launched and nothing is written.  NEOX_ERR_CUDA means a launch or allocation
@@ -77,6 +79,33 @@ typedef enum {
  */
 int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
                   void* out, float* lse, void* stream);
+
+/*
+ * Where the rotary embedding of Q and K is computed (the results are bit-identical):
+ *   NEOX_ROTATION_FUSED  inside the attention kernel, in shared memory, on every K tile
+ *                        each query unit streams (no extra HBM traffic; the K tile of a
+ *                        head is rotated once per query unit that reads it);
+ *   NEOX_ROTATION_PRE    by a separate pass that writes q' and k' (split hi/lo) once into
+ *                        the library's per-device scratch, 4*B*S*H*D bf16 values, which the
+ *                        attention kernel then loads instead of Q and K (needs
+ *                        rotary_dim % 16 == 0 and rotary_dim > 0);
+ *   NEOX_ROTATION_AUTO   PRE when rotary_dim >= 64 and rotary_dim % 16 == 0, else FUSED
+ *                        (the choice measured faster on B300 for the GPT-NeoX shapes).
+ */
+enum { NEOX_ROTATION_AUTO = 0, NEOX_ROTATION_FUSED = 1, NEOX_ROTATION_PRE = 2 };
+
+/*
+ * neox_attn_fwd with the rotation placement chosen by the caller (one of the
+ * NEOX_ROTATION_* values; anything else, or PRE with rotary_dim % 16 != 0 or
+ * rotary_dim == 0, gives NEOX_ERR_INVALID_ARG before any CUDA call).
+ * neox_attn_fwd(...) is neox_attn_fwd_ex(..., NEOX_ROTATION_AUTO, stream).
+ *
+ * The PRE placement uses the library's per-device scratch (allocated or grown on
+ * demand; growing synchronizes the device), which neox_attn_decode and neox_attn_bwd
+ * use too: calls that use it must not overlap on the GPU (order them on one stream).
+ */
+int neox_attn_fwd_ex(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
+                     void* out, float* lse, int rotation, void* stream);
 
 /*
  * Same contract as neox_attn_fwd, computed by the plain single-warpgroup tcgen05 kernel
