@@ -127,14 +127,15 @@ __device__ __forceinline__ int snake_unit(int round, int cta, int G) {
   return round * G + ((round & 1) ? (G - 1 - cta) : cta);
 }
 
-// PRE: the operands come pre-rotated (rope_prerotate_kernel: hi and lo of q' and k' in
-// the copy that tmap_rot views as [B, S, 4H, D]); the query tiles and K tiles are then
-// loaded with their side tiles by TMA and nothing is rotated here (r % 16 == 0 only).
+// PRE: the operands come pre-rotated (the pre-rotation pass: hi and lo of q' and k' in the
+// copy that tmap_rot views as [B, S, 4H, D], the lo slot in the side-tile layout); the
+// query tiles and K tiles are then loaded with their side tiles by TMA and nothing is
+// rotated here (rotary_dim % 16 == 0, or 24).
 template <int D, int RK, bool PRE>
 __global__ void __launch_bounds__(kWsThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rot,
                        const AttnParams p) {
-  static_assert(!PRE || (RK != kRotR24 && RK != kRotScalar), "pre-rotated operands need rotary_dim % 16 == 0");
+  static_assert(!PRE || RK != kRotScalar, "pre-rotated operands need rotary_dim % 16 == 0 or rotary_dim == 24");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NK = p.nk, NV = p.nv;
@@ -657,14 +658,16 @@ int launch_ws_impl(const CUtensorMap& map, const CUtensorMap& map_rot, AttnParam
   return 0;
 }
 
-// pre_rotated: map_rot views the rotated copy written by rope_prerotate_kernel (the caller
-// checks rotary_dim % 16 == 0 and rotary_dim > 0); otherwise map_rot is not read.
+// pre_rotated: map_rot views the rotated copy written by the pre-rotation pass (the caller
+// checks rotary_dim % 16 == 0 or rotary_dim == 24, rotary_dim > 0); otherwise map_rot is
+// not read.
 template <int D>
 int launch_attn_ws(const CUtensorMap& map, const CUtensorMap& map_rot, bool pre_rotated, const AttnParams& p,
                    int num_sms, cudaStream_t stream, int* last_err) {
   if (pre_rotated) {
     switch (rot_kind(p.r)) {
       case kRotR16: return launch_ws_impl<D, kRotR16, true>(map, map_rot, p, num_sms, stream, last_err);
+      case kRotR24: return launch_ws_impl<D, kRotR24, true>(map, map_rot, p, num_sms, stream, last_err);
       case kRotR32: return launch_ws_impl<D, kRotR32, true>(map, map_rot, p, num_sms, stream, last_err);
       case kRotGroups: return launch_ws_impl<D, kRotGroups, true>(map, map_rot, p, num_sms, stream, last_err);
       default: return -1;

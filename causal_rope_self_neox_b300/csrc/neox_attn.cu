@@ -293,10 +293,17 @@ int prerotate(Prepared& P, const void* qkv, cudaStream_t stream) {
   int rc = get_scratch(P.device, static_cast<size_t>(rows) * 4 * D * 2, 1, &scratch, &counters);
   if (rc != NEOX_OK) return rc;
   uint16_t* rot = reinterpret_cast<uint16_t*>(scratch);
-  const int64_t blocks = (rows + 7) / 8;
-  if (blocks > 0x7FFFFFFF) return NEOX_ERR_INVALID_ARG;
-  neox::rope_prerotate_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(qkv), rot, p.cs, rows, p.S, p.H, p.r);
+  if (p.r == 24) {
+    const int64_t blocks = (rows + 127) / 128;
+    if (blocks > 0x7FFFFFFF) return NEOX_ERR_INVALID_ARG;
+    neox::rope_prerotate_r24_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(qkv), rot, p.cs, rows, p.S, p.H);
+  } else {
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7FFFFFFF) return NEOX_ERR_INVALID_ARG;
+    neox::rope_prerotate_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(qkv), rot, p.cs, rows, p.S, p.H, p.r);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   rc = encode_rot_map(&P.map_rot, rot, p.B, p.S, p.H, D);
@@ -466,7 +473,7 @@ int neox_attn_fwd_ex(const void* qkv, int B, int S, int H, int D, int rotary_dim
   try {
     if (rotation != NEOX_ROTATION_AUTO && rotation != NEOX_ROTATION_FUSED && rotation != NEOX_ROTATION_PRE)
       return NEOX_ERR_INVALID_ARG;
-    const bool pre_ok = rotary_dim > 0 && rotary_dim % 16 == 0;
+    const bool pre_ok = rotary_dim > 0 && (rotary_dim % 16 == 0 || rotary_dim == 24);
     if (rotation == NEOX_ROTATION_PRE && !pre_ok) return NEOX_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Prepared P;

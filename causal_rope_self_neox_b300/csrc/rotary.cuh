@@ -298,6 +298,59 @@ __device__ __forceinline__ void rotate_two_rows_groups(uint8_t* tile, uint8_t* s
 // r % 16 == 0 (the side tiles then hold plain lo columns).  One warp per (b, s, h) row:
 // lanes 0..15 do q, lanes 16..31 do k, lane c of a half owns the 8-dim chunk c; a chunk
 // of the first half of the rotated dims also writes its partner chunk.
+// rotary_dim 24 (the GPT-NeoX-20B setting): the 24 rotated dims of a row in registers, as
+// rotate_row_small<3> does, and the lo slot laid out as the attention kernel's side tile
+// for r = 24: lo of dims 0..15, then one chunk holding the cross terms of dims 16..23 packed
+// ([lo | hi] for q', [hi | lo] for k'), zero beyond.  One thread per (row, q or k).
+template <int D>
+__device__ __forceinline__ void prerotate_r24(const uint16_t* __restrict__ src, uint16_t* __restrict__ hi,
+                                              uint16_t* __restrict__ lo, const float2* __restrict__ cs, int64_t pos,
+                                              bool is_q) {
+  constexpr int HH = 12;
+  float x[24], y[24];
+#pragma unroll
+  for (int c = 0; c < 3; ++c) unpack8(*reinterpret_cast<const uint4*>(src + 8 * c), x + 8 * c);
+  float4 t[6];
+  cs_load_n<6>(t, cs, HH, 0, pos);
+#pragma unroll
+  for (int i0 = 0; i0 < HH; i0 += 4) {  // same expressions as rotate_pairs8, four pairs at a time
+#pragma unroll
+    for (int i = i0; i < i0 + 4; ++i) {
+      const float cth = (i & 1) ? t[i >> 1].z : t[i >> 1].x;
+      const float sth = (i & 1) ? t[i >> 1].w : t[i >> 1].y;
+      y[i] = fmaf(x[i], cth, -x[i + HH] * sth);
+      y[i + HH] = fmaf(x[i + HH], cth, x[i] * sth);
+    }
+  }
+  uint4 h4[3], l4[3];
+#pragma unroll
+  for (int c = 0; c < 3; ++c) split8(y + 8 * c, h4[c], l4[c]);
+#pragma unroll
+  for (int c = 0; c < 3; ++c) *reinterpret_cast<uint4*>(hi + 8 * c) = h4[c];
+#pragma unroll
+  for (int c = 3; c < D / 8; ++c) *reinterpret_cast<uint4*>(hi + 8 * c) = *reinterpret_cast<const uint4*>(src + 8 * c);
+  *reinterpret_cast<uint4*>(lo + 0) = l4[0];
+  *reinterpret_cast<uint4*>(lo + 8) = l4[1];
+  *reinterpret_cast<uint4*>(lo + 16) = is_q ? l4[2] : h4[2];
+  *reinterpret_cast<uint4*>(lo + 24) = is_q ? h4[2] : l4[2];
+#pragma unroll
+  for (int c = 4; c < D / 8; ++c) *reinterpret_cast<uint4*>(lo + 8 * c) = make_uint4(0, 0, 0, 0);
+}
+
+// r = 24: one thread per (row, q or k), 256 threads = 128 rows per block.
+template <int D>
+__global__ void __launch_bounds__(256) rope_prerotate_r24_kernel(const uint16_t* __restrict__ qkv,
+                                                                 uint16_t* __restrict__ rot,
+                                                                 const float2* __restrict__ cs, int64_t rows, int S,
+                                                                 int H) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 128 + (threadIdx.x >> 1);
+  if (row >= rows) return;
+  const int which = threadIdx.x & 1;  // 0: q, 1: k
+  const int64_t pos = (row / H) % S;
+  uint16_t* hi = rot + row * 4 * D + 2 * which * D;
+  prerotate_r24<D>(qkv + row * 3 * D + which * D, hi, hi + D, cs, pos, which == 0);
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) rope_prerotate_kernel(const uint16_t* __restrict__ qkv, uint16_t* __restrict__ rot,
                                                              const float2* __restrict__ cs, int64_t rows, int S, int H,

@@ -88,7 +88,7 @@ int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, f
  *   NEOX_ROTATION_PRE    by a separate pass that writes q' and k' (split hi/lo) once into
  *                        the library's per-device scratch, 4*B*S*H*D bf16 values, which the
  *                        attention kernel then loads instead of Q and K (needs
- *                        rotary_dim % 16 == 0 and rotary_dim > 0);
+ *                        rotary_dim > 0 and rotary_dim % 16 == 0 or rotary_dim == 24);
  *   NEOX_ROTATION_AUTO   PRE when rotary_dim >= 64 and rotary_dim % 16 == 0, else FUSED
  *                        (the choice measured faster on B300 for the GPT-NeoX shapes).
  */
@@ -96,8 +96,9 @@ enum { NEOX_ROTATION_AUTO = 0, NEOX_ROTATION_FUSED = 1, NEOX_ROTATION_PRE = 2 };
 
 /*
  * neox_attn_fwd with the rotation placement chosen by the caller (one of the
- * NEOX_ROTATION_* values; anything else, or PRE with rotary_dim % 16 != 0 or
- * rotary_dim == 0, gives NEOX_ERR_INVALID_ARG before any CUDA call).
+ * NEOX_ROTATION_* values; anything else, or PRE with rotary_dim == 0 or a rotary_dim
+ * that is neither a multiple of 16 nor 24, gives NEOX_ERR_INVALID_ARG before any CUDA
+ * call).
  * neox_attn_fwd(...) is neox_attn_fwd_ex(..., NEOX_ROTATION_AUTO, stream).
  *
  * The PRE placement uses the library's per-device scratch (allocated or grown on

@@ -149,12 +149,13 @@ def test_bwd_invalid_arguments_rejected_before_cuda(lib, args, status):
 
 
 def test_rotation_placement_is_validated_before_any_cuda_call(lib):
-    # an unknown placement, and the pre-rotated one where it does not apply (rotary_dim % 16 != 0
-    # or no rotary dims), are rejected without touching the (fake) device addresses
+    # an unknown placement, and the pre-rotated one where it does not apply (rotary_dim neither
+    # a multiple of 16 nor 24, or no rotary dims), are rejected without touching the (fake)
+    # device addresses
     s = 0
     assert na.neox_attn_fwd_ex(A, 1, 128, 2, 64, 16, 1e4, OUT, LSE, 3, s) == na.NEOX_ERR_INVALID_ARG
     assert na.neox_attn_fwd_ex(A, 1, 128, 2, 64, 16, 1e4, OUT, LSE, -1, s) == na.NEOX_ERR_INVALID_ARG
-    assert na.neox_attn_fwd_ex(A, 1, 128, 2, 96, 24, 1e4, OUT, LSE, na.NEOX_ROTATION_PRE, s) \
+    assert na.neox_attn_fwd_ex(A, 1, 128, 2, 96, 40, 1e4, OUT, LSE, na.NEOX_ROTATION_PRE, s) \
         == na.NEOX_ERR_INVALID_ARG
     assert na.neox_attn_fwd_ex(A, 1, 128, 2, 64, 0, 1e4, OUT, LSE, na.NEOX_ROTATION_PRE, s) \
         == na.NEOX_ERR_INVALID_ARG

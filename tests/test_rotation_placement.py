@@ -26,6 +26,8 @@ def run(qkv_cpu, r, rotation):
 
 SHAPES = [
     (1, 130, 2, 64, 16, 1.0),     # ragged, one rotated chunk pair
+    (2, 300, 3, 96, 24, 1.0),     # r = 24: the packed cross-term chunk of the side tile
+    (1, 200, 2, 128, 24, 1.0),    # r = 24 at D = 128, ragged
     (2, 300, 3, 96, 32, 1.0),     # D = 96, two tiles, ragged
     (1, 640, 2, 96, 96, 1.0),     # every dim rotated at D = 96
     (3, 523, 2, 128, 64, 1.0),    # half rotary, several tiles
