@@ -140,8 +140,12 @@ int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary
  *
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that first call
- * before any stream capture.  Arguments, layouts, ownership and the other errors are
- * those of neox_attn_fwd.
+ * before any stream capture.  The CUDA driver may place the library's device code and
+ * this array on a device only when the library is first used there (lazy module
+ * loading), so make the first call on each device -- or any earlier call into the library
+ * there -- before the caller's allocator takes up the rest of the device's memory.
+ * Arguments, layouts, ownership and the other errors are those of neox_attn_fwd
+ * (the rotation is always computed inside the attention kernel).
  */
 int neox_attn_fwd_noalloc(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
                           void* out, float* lse, void* stream);

@@ -2,7 +2,7 @@
 the C ABI.  The forward's out and lse come from neox_attn_fwd on the same input.
 
 Tolerances per gradient slot (dq, dk, dv): max abs error <= 1.5e-2 of the slot's
-largest reference value, and RMS error <= 1e-2 of the reference's RMS.  They come from
+largest reference value, and RMS error <= 8e-3 of the reference's RMS.  They come from
 the kernel's rounding points (rotated q', k', the probabilities and ds rounded to bf16
 before the tensor cores, outputs rounded to bf16, fp32 everywhere else): restating
 those roundings in fp64 on CPU gives at most 6.0e-3 and 3.9e-3 on such shapes, and
@@ -17,7 +17,7 @@ from causal_rope_self_neox_b300.workloads import WORKLOADS, bf16_bits, make_qkv
 
 pytestmark = pytest.mark.gpu
 
-MAX_REL, REL_RMS = 1.5e-2, 1e-2
+MAX_REL, REL_RMS = 1.5e-2, 8e-3
 
 
 def make_dout(B, S, H, D, seed):

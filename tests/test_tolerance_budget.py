@@ -113,7 +113,7 @@ def test_plain_bf16_rotation_breaks_lse_tolerance():
 # probabilities P and ds to bf16 before its MMAs, takes delta from the forward's bf16
 # out and the fp32 lse, and writes bf16 gradients; everything else is fp32.  Restating
 # those rounding points in fp64 must stay well inside the GPU test's tolerances.
-BWD_MAX_REL, BWD_REL_RMS = 1.5e-2, 1e-2  # max abs error / max |ref|; RMS error / RMS ref
+BWD_MAX_REL, BWD_REL_RMS = 1.5e-2, 8e-3  # max abs error / max |ref|; RMS error / RMS ref
 
 
 def emulate_bwd(qkv, dout, r, base=10000.0):
