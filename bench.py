@@ -347,11 +347,17 @@ def run_ours(args, w):
     # the placement the library takes (the header's documented rule for "auto")
     pre = args.rotation == "pre" or (args.rotation == "auto" and w.rotary_dim >= 64 and w.rotary_dim % 16 == 0)
 
+    if args.alibi:
+        pre = False
+
     def step(q=qkv):
-        rc = na.neox_attn_fwd_ex(q.data_ptr(), w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, out.data_ptr(),
-                                 lse.data_ptr(), rotation, sh)
+        if args.alibi:
+            rc = na.neox_attn_fwd_alibi(q.data_ptr(), w.B, w.S, w.H, w.D, out.data_ptr(), lse.data_ptr(), sh)
+        else:
+            rc = na.neox_attn_fwd_ex(q.data_ptr(), w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, out.data_ptr(),
+                                     lse.data_ptr(), rotation, sh)
         if rc != 0:
-            raise na.NeoxAttnError(rc, "neox_attn_fwd_ex")
+            raise na.NeoxAttnError(rc, "neox_attn_fwd_alibi" if args.alibi else "neox_attn_fwd_ex")
 
     for _ in range(args.warmup):
         flush()
@@ -426,7 +432,7 @@ def run_ours(args, w):
     if rank == 0:
         peak, peak_sus, hbm, src = load_peaks()
         per_gpu = w.flops / (ms_per_step / 1e3) / 1e12
-        traffic, tsrc = profiled_traffic(("pre_" if pre else "") + w.name)
+        traffic, tsrc = profiled_traffic(("alibi_" if args.alibi else "pre_" if pre else "") + w.name)
         alg_bytes = 2 * w.B * w.S * w.H * 3 * w.D + 2 * w.B * w.S * w.H * w.D + 4 * w.B * w.H * w.S
         D = w.D
         line = {
@@ -434,8 +440,9 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, K x k_scale)",
             "config": {**w.describe(), "l2": L2_NOTE,
-                       "rotation": f"{args.rotation} -> " + ("pre-rotation pass + attention kernel" if pre
-                                                             else "fused in the attention kernel"),
+                       "rotation": ("none: ALiBi bias -m_h (i - j) instead (neox_attn_fwd_alibi)" if args.alibi else
+                                    f"{args.rotation} -> " + ("pre-rotation pass + attention kernel" if pre
+                                                              else "fused in the attention kernel")),
                        "parallelism": f"replicas x{world} (each rank its own workload; no collective on the data path)"},
             "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak, "unit": "TFLOP/s",
                          "frac": per_gpu / peak, "traffic": traffic,
@@ -457,7 +464,7 @@ def run_ours(args, w):
             "wall_s_timed_region": wall,
             "kernel_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and not args.alibi:
             line["cpu_baseline"] = cpu_baseline(w, qkv_cpu)
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -704,6 +711,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + sorted(DECODE_WORKLOADS), default="neox20b")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--alibi", action="store_true",
+                    help="time the ALiBi forward (neox_attn_fwd_alibi) on the workload's shape instead")
     ap.add_argument("--rotation", choices=["auto", "fused", "pre"], default="auto",
                     help="where the forward applies the rotary embedding (neox_attn_fwd_ex placement)")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",

@@ -29,7 +29,7 @@ NEOX_ROTATION_AUTO = 0
 NEOX_ROTATION_FUSED = 1
 NEOX_ROTATION_PRE = 2
 
-EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_ex", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
+EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_ex", "neox_attn_fwd_alibi", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
            "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
            "neox_attn_version", "neox_attn_fwd_noalloc", "neox_attn_decode", "neox_attn_bwd")
 
@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                 getattr(lib, name).restype = i32
             lib.neox_attn_fwd_ex.argtypes = [P, i32, i32, i32, i32, i32, f32, P, P, i32, P]
             lib.neox_attn_fwd_ex.restype = i32
+            lib.neox_attn_fwd_alibi.argtypes = [P, i32, i32, i32, i32, P, P, P]
+            lib.neox_attn_fwd_alibi.restype = i32
             lib.neox_attn_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
             lib.neox_attn_decode.restype = i32
             lib.neox_attn_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P]
@@ -91,6 +93,12 @@ def neox_attn_fwd_ex(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: i
     """Raw call with the rotation placement (NEOX_ROTATION_AUTO / _FUSED / _PRE)."""
     return load_library().neox_attn_fwd_ex(qkv_ptr, B, S, H, D, rotary_dim, rotary_base, out_ptr, lse_ptr, rotation,
                                            stream)
+
+
+def neox_attn_fwd_alibi(qkv_ptr: int, B: int, S: int, H: int, D: int, out_ptr: int, lse_ptr: int,
+                        stream: int = 0) -> int:
+    """Raw call of the ALiBi forward (no rotation; linear distance bias per head)."""
+    return load_library().neox_attn_fwd_alibi(qkv_ptr, B, S, H, D, out_ptr, lse_ptr, stream)
 
 
 def neox_attn_fwd_simple(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
@@ -187,6 +195,29 @@ def attn_fwd(qkv, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=N
                                       lse.data_ptr(), stream.cuda_stream)
     if rc != NEOX_OK:
         raise NeoxAttnError(rc, "neox_attn_fwd")
+    return out, lse
+
+
+def attn_fwd_alibi(qkv, out=None, lse=None, stream=None):
+    """Causal attention with the ALiBi bias (no rotation) on CUDA tensors: ``qkv`` bf16
+    ``[B, S, H, 3, D]``.  Returns ``(out[B,S,H,D] bf16, lse[B,H,S] fp32)``."""
+    import torch
+
+    if qkv.dim() != 5 or qkv.shape[3] != 3 or qkv.dtype != torch.bfloat16 or not qkv.is_cuda:
+        raise ValueError("qkv must be a CUDA bf16 tensor of shape [B, S, H, 3, D]")
+    if not qkv.is_contiguous():
+        raise ValueError("qkv must be contiguous")
+    B, S, H, _, D = qkv.shape
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=qkv.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=qkv.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device)
+    with torch.cuda.device(qkv.device):
+        rc = neox_attn_fwd_alibi(qkv.data_ptr(), B, S, H, D, out.data_ptr(), lse.data_ptr(), stream.cuda_stream)
+    if rc != NEOX_OK:
+        raise NeoxAttnError(rc, "neox_attn_fwd_alibi")
     return out, lse
 
 

@@ -131,11 +131,16 @@ __device__ __forceinline__ int snake_unit(int round, int cta, int G) {
 // copy that tmap_rot views as [B, S, 4H, D], the lo slot in the side-tile layout); the
 // query tiles and K tiles are then loaded with their side tiles by TMA and nothing is
 // rotated here (rotary_dim % 16 == 0, or 24).
-template <int D, int RK, bool PRE>
+//
+// ALIBI: no rotation; the scores get the linear position bias -m_h (i - j) of the ALiBi
+// scheme instead (m_h the head's slope: 2^(-8k/n), k = 1..n, for the n = largest power of
+// two <= H heads, then 2^(-8k/(2n)) for odd k for the rest).
+template <int D, int RK, bool PRE, bool ALIBI = false>
 __global__ void __launch_bounds__(kWsThreads, 1)
     attn_fwd_ws_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_rot,
                        const AttnParams p) {
   static_assert(!PRE || RK != kRotScalar, "pre-rotated operands need rotary_dim % 16 == 0 or rotary_dim == 24");
+  static_assert(!ALIBI || (RK == kRotNone && !PRE), "the ALiBi bias replaces the rotary embedding");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NK = p.nk, NV = p.nv;
@@ -499,6 +504,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       if (n == 0) continue;
       const int qt = 2 * u.t + tau;
       float m_used = -INFINITY, l_run = 0.0f;
+      // ALiBi: the head's slope in log2 units, and the bias of column 0 of block 0 for this
+      // thread's row (the bias of key k is bh * (k - row), at most 0 on the causal side)
+      float bh = 0.0f, row0 = 0.0f;
+      if constexpr (ALIBI) {
+        int n2 = 1;
+        while (n2 * 2 <= p.H) n2 *= 2;
+        const double e = u.h < n2 ? -8.0 * (u.h + 1) / n2 : -8.0 * (2 * (u.h - n2) + 1) / (2.0 * n2);
+        bh = static_cast<float>(exp2(e) * 1.4426950408889634);
+        row0 = -bh * static_cast<float>(qt * kRows + row);
+      }
       // every exit decision is warp-uniform: the TMEM loads and stores below are
       // warp-collective, so no lane may leave while the others go on
       bool ok = true;
@@ -512,7 +527,39 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         tc_fence_after_sync();
         uint32_t sr[128];
         float mx;
-        if (j != qt) {
+        if constexpr (ALIBI) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, sr + c * 32);
+          tmem_wait_ld();
+          // biased scores in log2 units: s * log2(e)/sqrt(D) + bh * (128 j + c - row)
+          const uint64_t sc2 = f32x2_pack(sl2, sl2), bh2 = f32x2_pack(bh, bh);
+          const float off = fmaf(bh, static_cast<float>(j * kRows), row0);
+          const uint64_t off2 = f32x2_pack(off, off);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const uint64_t b = ffma2(f32x2_pack(static_cast<float>(2 * c), static_cast<float>(2 * c + 1)), bh2, off2);
+            const uint64_t v = ffma2(f32x2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sc2, b);
+            float v0, v1;
+            f32x2_unpack(v, v0, v1);
+            sr[2 * c] = __float_as_uint(v0);
+            sr[2 * c + 1] = __float_as_uint(v1);
+          }
+          if (j == qt) {
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c > row) sr[c] = __float_as_uint(-INFINITY);
+          }
+          float mc[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t* v = sr + 16 * g;
+            float m = fmax3f(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+            for (int q = 3; q < 15; q += 2) m = fmax3f(m, __uint_as_float(v[q]), __uint_as_float(v[q + 1]));
+            mc[g] = fmaxf(m, __uint_as_float(v[15]));
+          }
+          mx = fmaxf(fmax3f(mc[0], mc[1], mc[2]), fmax3f(fmax3f(mc[3], mc[4], mc[5]), mc[6], mc[7]));
+        } else if (j != qt) {
           // below the diagonal: the loads return each 32-column chunk's max as well
           float mq[4];
 #pragma unroll
@@ -539,7 +586,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           }
           mx = fmaxf(fmax3f(mc[0], mc[1], mc[2]), fmax3f(fmax3f(mc[3], mc[4], mc[5]), mc[6], mc[7]));
         }
-        const float mx_s = mx * sl2;
+        const float mx_s = ALIBI ? mx : mx * sl2;  // the biased scores are in log2 units already
         float m_new = m_used;
         bool rescale = false;
         if (j == 0) {
@@ -550,7 +597,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         const float alpha = rescale ? ex2_approx(m_used - m_new) : 1.0f;
         // p = 2^(s * log2(e)/sqrt(D) - m): packed fp32 FMA, MUFU exp2, four packed partial sums
-        const uint64_t sc2 = f32x2_pack(sl2, sl2), nm2 = f32x2_pack(-m_new, -m_new);
+        const float sc = ALIBI ? 1.0f : sl2;
+        const uint64_t sc2 = f32x2_pack(sc, sc), nm2 = f32x2_pack(-m_new, -m_new);
         uint64_t acc[4] = {0, 0, 0, 0};
         uint32_t pk[64];
 #pragma unroll
@@ -641,12 +689,12 @@ inline void pick_rings(int D, int side_cols, int* nk, int* nv) {
   *nk = *nv = 1;
 }
 
-template <int D, int RK, bool PRE>
+template <int D, int RK, bool PRE, bool ALIBI = false>
 int launch_ws_impl(const CUtensorMap& map, const CUtensorMap& map_rot, AttnParams p, int num_sms, cudaStream_t stream,
                    int* last_err) {
   pick_rings(D, p.side_cols, &p.nk, &p.nv);
   const WsLayout L = ws_layout(D, p.side_cols, p.nk, p.nv);
-  auto kern = attn_fwd_ws_kernel<D, RK, PRE>;
+  auto kern = attn_fwd_ws_kernel<D, RK, PRE, ALIBI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total());
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   const int T = (p.S + 255) / 256;
@@ -656,6 +704,13 @@ int launch_ws_impl(const CUtensorMap& map, const CUtensorMap& map_rot, AttnParam
   e = cudaGetLastError();
   if (e != cudaSuccess) { *last_err = static_cast<int>(e); return -4; }
   return 0;
+}
+
+// The ALiBi variant (rotary_dim 0 in p).
+template <int D>
+int launch_attn_ws_alibi(const CUtensorMap& map, const AttnParams& p, int num_sms, cudaStream_t stream,
+                         int* last_err) {
+  return launch_ws_impl<D, kRotNone, false, true>(map, map, p, num_sms, stream, last_err);
 }
 
 // pre_rotated: map_rot views the rotated copy written by the pre-rotation pass (the caller

@@ -503,6 +503,25 @@ int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, f
   return neox_attn_fwd_ex(qkv, B, S, H, D, rotary_dim, rotary_base, out, lse, NEOX_ROTATION_AUTO, stream);
 }
 
+int neox_attn_fwd_alibi(const void* qkv, int B, int S, int H, int D, void* out, float* lse, void* stream) {
+  try {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Prepared P;
+    // no rotary dims (so no table): the base is only validated, never used
+    int rc = prepare(qkv, B, S, H, D, 0, 10000.0f, out, lse, st, &P);
+    if (rc != NEOX_OK) return rc;
+    int r2 = 0;
+    switch (D) {
+      case 64: r2 = neox::launch_attn_ws_alibi<64>(P.map, P.p, P.dev.num_sms, st, &g_last_cuda_error); break;
+      case 96: r2 = neox::launch_attn_ws_alibi<96>(P.map, P.p, P.dev.num_sms, st, &g_last_cuda_error); break;
+      default: r2 = neox::launch_attn_ws_alibi<128>(P.map, P.p, P.dev.num_sms, st, &g_last_cuda_error); break;
+    }
+    return r2 == 0 ? NEOX_OK : NEOX_ERR_CUDA;
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
+
 int neox_attn_fwd_simple(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base, void* out,
                          float* lse, void* stream) {
   try {

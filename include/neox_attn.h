@@ -109,6 +109,21 @@ int neox_attn_fwd_ex(const void* qkv, int B, int S, int H, int D, int rotary_dim
                      void* out, float* lse, int rotation, void* stream);
 
 /*
+ * ALiBi variant of the forward: the other positional scheme GPT-NeoX supports ("gpt-neox -
+ * 模型与框架" hub page, sections "架构创新" and "位置编码"; GPT-NeoX library summary, "Key
+ * capabilities": rotary and ALiBi position embeddings).  No rotation; instead each score
+ * gets a linear bias by query-key distance:
+ *   s_ij = q_i.k_j / sqrt(D) - m_h (i - j)   for j <= i,
+ * with the head slopes of the published ALiBi method (the pages name the scheme but print
+ * no formula): for the n = largest power of two <= H heads m_h = 2^(-8(h+1)/n), h < n;
+ * the remaining heads take 2^(-8k/(2n)) for odd k = 1, 3, 5, ... in order.
+ * out_i = sum_j softmax_j(s_ij) v_j and lse_i = ln sum_j exp(s_ij), as in neox_attn_fwd.
+ * Arguments, layouts, ownership and errors are those of neox_attn_fwd (no rotary
+ * arguments; no table is built).
+ */
+int neox_attn_fwd_alibi(const void* qkv, int B, int S, int H, int D, void* out, float* lse, void* stream);
+
+/*
  * Same contract as neox_attn_fwd, computed by the plain single-warpgroup tcgen05 kernel
  * (one CTA per 128-row query tile, every stage in sequence).  Slower; kept as an
  * independent second implementation of the same tile layouts for cross-checking.
