@@ -57,6 +57,8 @@ def _load():
             lib.neox_oracle_decode.restype = i32
             lib.neox_oracle_bwd.argtypes = [P, P, i32, i32, i32, i32, i32, f64, P, i32]
             lib.neox_oracle_bwd.restype = i32
+            lib.neox_oracle_qkv_proj.argtypes = [P, P, P, ctypes.c_int64, i32, i32, P, ctypes.c_int64, P, i32]
+            lib.neox_oracle_qkv_proj.restype = i32
             lib.neox_oracle_alibi_slopes.argtypes = [i32, P]
             lib.neox_oracle_alibi_slopes.restype = None
             lib.neox_oracle_fwd_alibi.argtypes = [P, i32, i32, i32, i32, P, P, i32]
@@ -177,6 +179,53 @@ def bwd(qkv_bits: np.ndarray, dout_bits: np.ndarray, B: int, S: int, H: int, D: 
     if rc != 0:
         raise ValueError(f"oracle backward failed ({rc})")
     return dqkv
+
+
+def qkv_proj(x_bits: np.ndarray, w_bits: np.ndarray, bias_bits=None, rows=None, threads: int | None = None):
+    """The fused query_key_value projection in fp64: ``x[M,K] @ w[K,N] + bias[N]`` from the
+    bf16 bits (``w`` laid out [hidden, H, 3, D] flattened to [K, N]).  ``rows``: token rows
+    to compute (default all).  Returns fp64 ``[n_rows, N]``."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    M, K = x.shape
+    K2, N = w.shape
+    if K2 != K:
+        raise ValueError("x and w disagree on the hidden size")
+    b = None if bias_bits is None else np.ascontiguousarray(bias_bits, dtype=np.uint16)
+    if b is not None and b.shape != (N,):
+        raise ValueError("bias must have N entries")
+    R = None if rows is None else np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+    n = M if R is None else R.shape[0]
+    out = np.empty((n, N), dtype=np.float64)
+    rc = _load().neox_oracle_qkv_proj(_ptr(x), _ptr(w), None if b is None else _ptr(b), M, K, N,
+                                      None if R is None else _ptr(R), 0 if R is None else n, _ptr(out),
+                                      threads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"neox_oracle_qkv_proj failed: {rc}")
+    return out
+
+
+def qkv_proj_rotated(x_bits: np.ndarray, w_bits: np.ndarray, bias_bits, B: int, S: int, H: int, D: int,
+                     rotary_dim: int, base: float = 10000.0, rows=None, threads: int | None = None) -> np.ndarray:
+    """The projection followed by the rotary embedding of its query and key slots, in fp64.
+
+    Tokens are ``x`` rows ``t = b*S + s`` (position ``s``).  Each token's projection
+    ``qkv_proj`` row is read as ``[H, 3, D]`` (slot 0 = query, 1 = key, 2 = value); the query
+    and key vectors of every head are rotated by ``rotate`` at the token's position, the
+    value vectors are left as they are.  ``rows``: token rows to compute (default all).
+    Returns fp64 ``[n_rows, H, 3, D]``.
+    """
+    if x_bits.shape[0] != B * S:
+        raise ValueError("x must hold B*S token rows")
+    y = qkv_proj(x_bits, w_bits, bias_bits, rows=rows, threads=threads).reshape(-1, H, 3, D)
+    toks = np.arange(B * S, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64).reshape(-1)
+    if rotary_dim:
+        for n, t in enumerate(toks):
+            pos = int(t % S)
+            for h in range(H):
+                for slot in (0, 1):
+                    y[n, h, slot] = rotate(y[n, h, slot], pos, rotary_dim, base)
+    return y
 
 
 def alibi_slopes(H: int) -> np.ndarray:

@@ -33,6 +33,9 @@
  * weighted sum of v_j;  lse = max + ln(sum).
  * The backward (neox_oracle_bwd, at the end) applies the chain rule to those same
  * steps, in reverse, for the gradient of sum(dout * out) with respect to qkv.
+ * The query_key_value projection that produces the packed qkv (neox_oracle_qkv_proj,
+ * last in the file) is one plain product of the token rows with the weight plus the
+ * layer's bias, read from the same guide's layer list and HuggingFace weight layout.
  */
 #include <math.h>
 #include <pthread.h>
@@ -683,5 +686,97 @@ int neox_oracle_fwd_alibi(const uint16_t* qkv, int B, int S, int H, int D, doubl
   for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
   pthread_mutex_destroy(&J.mu);
   free(slopes);
+  return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * Fused query_key_value projection (the step just before the attention).
+ *
+ * "GPT-NeoX on FasterTransformer" guide, section "从 HuggingFace 检查点部署": the
+ * HuggingFace checkpoint stores attention.query_key_value.weight as
+ * [hidden_size, num_heads, 3, head_hidden], so output feature n = (h*3 + slot)*D + d of
+ * token t is sum_k x[t,k] * w[k,n], and the tokens' outputs form the packed qkv
+ * [B,S,H,3,D] the attention reads.  The layer list on the same page
+ * ("attention.query_key_value.*") includes its bias, added to every token (optional
+ * here: bias == NULL means none).
+ *
+ *   out[t, n] = sum_{k < K} x[t, k] * w[k, n] + bias[n]      (fp64, exact bf16 inputs)
+ *
+ * x: bf16 bits [M, K] (token-major), w: bf16 bits [K, N], bias: bf16 bits [N] or NULL,
+ * out: fp64 [n_rows, N] for the listed token rows (rows == NULL: all M rows in order).
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const uint16_t* x;
+  const uint16_t* w;
+  const uint16_t* bias;
+  int64_t M;
+  int K, N;
+  const int64_t* rows;
+  int64_t n_rows;
+  double* out;
+  pthread_mutex_t mu;
+  int64_t next;
+  int failed;
+} pjob_t;
+
+static void* worker_proj(void* arg) {
+  pjob_t* J = (pjob_t*)arg;
+  const int K = J->K, N = J->N;
+  double* xr = malloc(sizeof(double) * (size_t)K);
+  if (!xr) {
+    pthread_mutex_lock(&J->mu);
+    J->failed = 1;
+    pthread_mutex_unlock(&J->mu);
+    return NULL;
+  }
+  for (;;) {
+    pthread_mutex_lock(&J->mu);
+    int64_t it = J->next++;
+    pthread_mutex_unlock(&J->mu);
+    if (it >= J->n_rows) break;
+    const int64_t t = J->rows ? J->rows[it] : it;
+    for (int k = 0; k < K; ++k) xr[k] = bf16_to_f64(J->x[t * K + k]);
+    double* o = J->out + it * (int64_t)N;
+    for (int n = 0; n < N; ++n) o[n] = J->bias ? bf16_to_f64(J->bias[n]) : 0.0;
+    for (int k = 0; k < K; ++k) {
+      const uint16_t* wk = J->w + (int64_t)k * N;
+      const double a = xr[k];
+      for (int n = 0; n < N; ++n) o[n] += a * bf16_to_f64(wk[n]);
+    }
+  }
+  free(xr);
+  return NULL;
+}
+
+int neox_oracle_qkv_proj(const uint16_t* x, const uint16_t* w, const uint16_t* bias, int64_t M, int K, int N,
+                         const int64_t* rows, int64_t n_rows, double* out, int threads) {
+  if (!x || !w || !out || M < 1 || K < 1 || N < 1) return ORACLE_ERR_ARG;
+  if (rows) {
+    for (int64_t i = 0; i < n_rows; ++i)
+      if (rows[i] < 0 || rows[i] >= M) return ORACLE_ERR_ARG;
+  } else {
+    n_rows = M;
+  }
+  pjob_t J;
+  memset(&J, 0, sizeof J);
+  J.x = x;
+  J.w = w;
+  J.bias = bias;
+  J.M = M;
+  J.K = K;
+  J.N = N;
+  J.rows = rows;
+  J.n_rows = n_rows;
+  J.out = out;
+  pthread_mutex_init(&J.mu, NULL);
+  if (threads < 1) threads = 1;
+  if (threads > 256) threads = 256;
+  pthread_t tid[256];
+  int started = 0;
+  for (int t = 0; t < threads; ++t)
+    if (pthread_create(&tid[t], NULL, worker_proj, &J) == 0) ++started;
+  if (started == 0) worker_proj(&J);
+  for (int t = 0; t < started; ++t) pthread_join(tid[t], NULL);
+  pthread_mutex_destroy(&J.mu);
   return J.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }
