@@ -29,7 +29,7 @@ NEOX_ROTATION_AUTO = 0
 NEOX_ROTATION_FUSED = 1
 NEOX_ROTATION_PRE = 2
 
-EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_ex", "neox_attn_fwd_alibi", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
+EXPORTS = ("neox_attn_fwd", "neox_attn_fwd_ex", "neox_attn_fwd_alibi", "neox_attn_qkv_proj", "neox_attn_fwd_simple", "neox_attn_get_device_error", "neox_attn_status_string",
            "neox_attn_last_cuda_error", "neox_attn_release", "neox_attn_selftest_wait_timeout",
            "neox_attn_version", "neox_attn_fwd_noalloc", "neox_attn_decode", "neox_attn_bwd")
 
@@ -60,6 +60,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
             lib.neox_attn_fwd_ex.restype = i32
             lib.neox_attn_fwd_alibi.argtypes = [P, i32, i32, i32, i32, P, P, P]
             lib.neox_attn_fwd_alibi.restype = i32
+            lib.neox_attn_qkv_proj.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P]
+            lib.neox_attn_qkv_proj.restype = i32
             lib.neox_attn_decode.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, P]
             lib.neox_attn_decode.restype = i32
             lib.neox_attn_bwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, P]
@@ -99,6 +101,14 @@ def neox_attn_fwd_alibi(qkv_ptr: int, B: int, S: int, H: int, D: int, out_ptr: i
                         stream: int = 0) -> int:
     """Raw call of the ALiBi forward (no rotation; linear distance bias per head)."""
     return load_library().neox_attn_fwd_alibi(qkv_ptr, B, S, H, D, out_ptr, lse_ptr, stream)
+
+
+def neox_attn_qkv_proj(x_ptr: int, w_ptr: int, bias_ptr: int, B: int, S: int, hidden: int, H: int, D: int,
+                       rotary_dim: int, rotary_base: float, qkv_ptr: int, stream: int = 0) -> int:
+    """Raw call of the query_key_value projection (bias_ptr 0 = no bias; rotary_dim > 0
+    rotates the query/key slots of the result)."""
+    return load_library().neox_attn_qkv_proj(x_ptr, w_ptr, bias_ptr or None, B, S, hidden, H, D, rotary_dim,
+                                             rotary_base, qkv_ptr, stream)
 
 
 def neox_attn_fwd_simple(qkv_ptr: int, B: int, S: int, H: int, D: int, rotary_dim: int, rotary_base: float,
@@ -219,6 +229,34 @@ def attn_fwd_alibi(qkv, out=None, lse=None, stream=None):
     if rc != NEOX_OK:
         raise NeoxAttnError(rc, "neox_attn_fwd_alibi")
     return out, lse
+
+
+def qkv_proj(x, w, bias, B: int, S: int, H: int, D: int, rotary_dim: int = 0, rotary_base: float = 10000.0,
+             out=None, stream=None):
+    """The query_key_value projection on CUDA tensors: ``x`` bf16 ``[B*S, hidden]`` (or
+    ``[B, S, hidden]``), ``w`` bf16 ``[hidden, H, 3, D]`` (or ``[hidden, 3*H*D]``), ``bias``
+    bf16 ``[3*H*D]`` or None.  Returns the packed ``qkv[B, S, H, 3, D]`` bf16, its query and
+    key slots rotated when ``rotary_dim > 0``."""
+    import torch
+
+    for name, t in (("x", x), ("w", w)) + ((("bias", bias),) if bias is not None else ()):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+    hidden = x.shape[-1]
+    if x.numel() != B * S * hidden or w.numel() != hidden * 3 * H * D or w.shape[0] != hidden:
+        raise ValueError("x must be [B*S, hidden] and w [hidden, H, 3, D]")
+    if bias is not None and bias.numel() != 3 * H * D:
+        raise ValueError("bias must have 3*H*D entries")
+    if out is None:
+        out = torch.empty((B, S, H, 3, D), dtype=torch.bfloat16, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        rc = neox_attn_qkv_proj(x.data_ptr(), w.data_ptr(), 0 if bias is None else bias.data_ptr(), B, S, hidden, H,
+                                D, rotary_dim, rotary_base, out.data_ptr(), stream.cuda_stream)
+    if rc != NEOX_OK:
+        raise NeoxAttnError(rc, "neox_attn_qkv_proj")
+    return out
 
 
 def attn_decode(qkv_new, k_cache, v_cache, pos, rotary_dim: int, rotary_base: float = 10000.0, out=None, lse=None,

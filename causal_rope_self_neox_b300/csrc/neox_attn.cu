@@ -17,6 +17,7 @@
 #include "attn_ws.cuh"
 #include "decode.cuh"
 #include "attn_bwd.cuh"
+#include "qkv_proj.cuh"
 
 namespace {
 
@@ -153,6 +154,41 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return NEOX_OK;
+}
+
+// 2-D bf16 map over a row-major [outer, inner] matrix, 128-byte swizzle.
+int encode_2d_sw128(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                    uint32_t box_outer) {
+  if (!resolve_encode()) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return NEOX_OK;
+}
+
+int validate_proj(const void* x, const void* w, const void* bias, int B, int S, int hidden, int H, int D, int r,
+                  float base, const void* qkv) {
+  if (!x || !w || !qkv) return NEOX_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || hidden < 8 || (hidden & 7)) return NEOX_ERR_INVALID_ARG;
+  if (D != 64 && D != 96 && D != 128) return NEOX_ERR_UNSUPPORTED_HEAD_DIM;
+  if (r < 0 || r > D || (r & 1)) return NEOX_ERR_INVALID_ARG;
+  if (!(base > 0.0f) || !std::isfinite(base)) return NEOX_ERR_INVALID_ARG;
+  const uint64_t M = static_cast<uint64_t>(B) * S, N = static_cast<uint64_t>(3) * H * D;
+  if (M > 0x7FFFFFFFull || N > 0x7FFFFFFFull) return NEOX_ERR_INVALID_ARG;
+  if (M * hidden >= (1ull << 40) || N * hidden >= (1ull << 40) || M * N >= (1ull << 40)) return NEOX_ERR_INVALID_ARG;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), wa = reinterpret_cast<uintptr_t>(w),
+                  ba = reinterpret_cast<uintptr_t>(bias), oa = reinterpret_cast<uintptr_t>(qkv);
+  if ((xa & 15) || (wa & 15) || (ba & 15) || (oa & 15)) return NEOX_ERR_MISALIGNED;
+  const uint64_t out_bytes = M * N * 2;
+  if (ranges_overlap(oa, out_bytes, xa, M * hidden * 2) || ranges_overlap(oa, out_bytes, wa, N * hidden * 2) ||
+      (bias && ranges_overlap(oa, out_bytes, ba, N * 2)))
+    return NEOX_ERR_INVALID_ARG;
   return NEOX_OK;
 }
 
@@ -517,6 +553,39 @@ int neox_attn_fwd_alibi(const void* qkv, int B, int S, int H, int D, void* out, 
       default: r2 = neox::launch_attn_ws_alibi<128>(P.map, P.p, P.dev.num_sms, st, &g_last_cuda_error); break;
     }
     return r2 == 0 ? NEOX_OK : NEOX_ERR_CUDA;
+  } catch (...) {
+    return NEOX_ERR_CUDA;
+  }
+}
+
+int neox_attn_qkv_proj(const void* x, const void* w, const void* bias, int B, int S, int hidden, int H, int D,
+                       int rotary_dim, float rotary_base, void* qkv, void* stream) {
+  try {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int rc = validate_proj(x, w, bias, B, S, hidden, H, D, rotary_dim, rotary_base, qkv);
+    if (rc != NEOX_OK) return rc;
+    int device = 0;
+    DeviceInfo dev;
+    if ((rc = current_device(&device, &dev)) != NEOX_OK) return rc;
+    neox::ProjParams p{};
+    p.bias = static_cast<const uint16_t*>(bias);
+    p.cs = nullptr;
+    if (rotary_dim > 0 && (rc = get_table(device, S, rotary_dim, rotary_base, st, &p.cs)) != NEOX_OK) return rc;
+    p.M = B * S;
+    p.N = 3 * H * D;
+    p.K = hidden;
+    p.S = S;
+    p.D = D;
+    p.r = rotary_dim;
+    p.num_m = (p.M + 127) / 128;
+    const int NT = neox::proj_tile_n(D);
+    p.num_tiles = p.num_m * ((p.N + NT - 1) / NT);
+    p.wait_limit_ns = neox::kWaitLimitNs;
+    CUtensorMap mx, mw, mo;
+    if ((rc = encode_2d_sw128(&mx, x, hidden, p.M, 64, 128)) != NEOX_OK) return rc;
+    if ((rc = encode_2d_sw128(&mw, w, p.N, hidden, 64, 64)) != NEOX_OK) return rc;
+    if ((rc = encode_2d_sw128(&mo, qkv, p.N, p.M, 64, 32)) != NEOX_OK) return rc;
+    return neox::launch_qkv_proj(mx, mw, mo, p, dev.num_sms, st, &g_last_cuda_error) == 0 ? NEOX_OK : NEOX_ERR_CUDA;
   } catch (...) {
     return NEOX_ERR_CUDA;
   }

@@ -164,3 +164,26 @@ def decode_from_sequence(qkv: torch.Tensor, pos, Smax: int):
         kc[b, :, :p] = qkv[b, :p, :, 1].permute(1, 0, 2)
         vc[b, :, :p] = qkv[b, :p, :, 2].permute(1, 0, 2)
     return new, kc, vc
+
+
+# ------------------------------------------------------- qkv projection ----
+# The query_key_value projection that feeds the attention: token rows x[B*S, hidden] (the
+# layer-normed hidden states), weight w[hidden, H, 3, D] (HuggingFace layout) and bias[3*H*D].
+# hidden = H * D for the GPT-NeoX family (6144 = 64 x 96 for the 20B model).
+# Recipe: one torch.Generator seeded with ``seed``; x ~ N(0, 1); w ~ N(0, 1) / sqrt(hidden)
+# (so the projections are about unit-normal, the scale of the attention inputs above);
+# bias ~ N(0, 0.5^2); each drawn in fp32 and cast to bf16 (round to nearest even).
+
+def make_proj_inputs(B: int, S: int, hidden: int, H: int, D: int, seed: int, with_bias: bool = True):
+    """``(x[B*S, hidden], w[hidden, 3*H*D], bias[3*H*D] or None)`` bf16 on the CPU."""
+    g = torch.Generator().manual_seed(int(seed))
+    N = 3 * H * D
+    x = torch.randn((B * S, hidden), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    w = (torch.randn((hidden, N), generator=g, dtype=torch.float32) / float(np.sqrt(hidden))).to(torch.bfloat16)
+    bias = (torch.randn((N,), generator=g, dtype=torch.float32) * 0.5).to(torch.bfloat16) if with_bias else None
+    return x, w, bias
+
+
+def proj_inputs(w: Workload, with_bias: bool = True):
+    """The projection inputs of an attention workload: hidden = H * D, seed 3000 + index."""
+    return make_proj_inputs(w.B, w.S, w.H * w.D, w.H, w.D, 3000 + w.index, with_bias)

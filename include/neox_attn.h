@@ -124,6 +124,37 @@ int neox_attn_fwd_ex(const void* qkv, int B, int S, int H, int D, int rotary_dim
 int neox_attn_fwd_alibi(const void* qkv, int B, int S, int H, int D, void* out, float* lse, void* stream);
 
 /*
+ * The fused query_key_value projection that produces the packed qkv, with its bias and,
+ * when rotary_dim > 0, the NeoX rotary embedding of the query and key slots applied on the
+ * way out ("GPT-NeoX on FasterTransformer" guide: section "从 HuggingFace 检查点部署" gives
+ * the weight layout [hidden_size, num_heads, 3, head_hidden], the layer list in
+ * "从 EleutherAI 检查点部署" gives attention.query_key_value's weight and bias, and
+ * "模型配置（config.ini）" the 20B shape: hidden 6144 = 64 heads x 96, rotary_embedding 24).
+ *
+ *   x     device, bf16 [B*S, hidden] row-major: token t = b*S + s is at position s.
+ *   w     device, bf16 [hidden, H, 3, D] row-major (= [hidden, N], N = 3*H*D).
+ *   bias  device, bf16 [N], or NULL for none.
+ *   qkv   device, bf16 [B, S, H, 3, D] (= [B*S, N]), written:
+ *           y[t, n] = bf16( sum_k x[t,k] * w[k,n] + bias[n] )   (fp32 accumulation)
+ *         and then, if rotary_dim > 0, for every head's query and key slot and each
+ *         i < rotary_dim/2, with a = y[.., i], b = y[.., i + rotary_dim/2] and
+ *         theta = s * rotary_base^(-2i/rotary_dim):
+ *           y[.., i] = bf16(a cos(theta) - b sin(theta)),
+ *           y[.., i + rotary_dim/2] = bf16(b cos(theta) + a sin(theta)),
+ *         (rotation in fp32 of the bf16 projection, rounded once more); value slots and
+ *         dims >= rotary_dim are the plain projection.  A qkv written with rotary_dim > 0
+ *         is already rotated: give it to neox_attn_fwd with rotary_dim 0.
+ * Sizes: hidden a multiple of 8 (>= 8); D in {64, 96, 128}; 0 <= rotary_dim <= D, even;
+ * B*S and N below 2^31.  All pointers 16-byte aligned; qkv may not overlap x, w or bias.
+ * Errors as neox_attn_fwd: NEOX_ERR_INVALID_ARG / _UNSUPPORTED_HEAD_DIM / _MISALIGNED
+ * before any CUDA call; NEOX_ERR_CUDA if a launch or the cos/sin table (cached per device,
+ * rotary_dim and base, shared with the attention calls) fails; a device-side timeout shows
+ * in neox_attn_get_device_error().  Asynchronous on `stream`; the caller owns all buffers.
+ */
+int neox_attn_qkv_proj(const void* x, const void* w, const void* bias, int B, int S, int hidden, int H, int D,
+                       int rotary_dim, float rotary_base, void* qkv, void* stream);
+
+/*
  * Same contract as neox_attn_fwd, computed by the plain single-warpgroup tcgen05 kernel
  * (one CTA per 128-row query tile, every stage in sequence).  Slower; kept as an
  * independent second implementation of the same tile layouts for cross-checking.

@@ -205,19 +205,31 @@ def qkv_proj(x_bits: np.ndarray, w_bits: np.ndarray, bias_bits=None, rows=None, 
     return out
 
 
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """fp64 -> nearest bf16 (ties to even) -> fp64, through torch's conversion."""
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64)).to(torch.bfloat16).double().numpy()
+
+
 def qkv_proj_rotated(x_bits: np.ndarray, w_bits: np.ndarray, bias_bits, B: int, S: int, H: int, D: int,
-                     rotary_dim: int, base: float = 10000.0, rows=None, threads: int | None = None) -> np.ndarray:
+                     rotary_dim: int, base: float = 10000.0, rows=None, threads: int | None = None,
+                     bf16_steps: bool = False) -> np.ndarray:
     """The projection followed by the rotary embedding of its query and key slots, in fp64.
 
     Tokens are ``x`` rows ``t = b*S + s`` (position ``s``).  Each token's projection
     ``qkv_proj`` row is read as ``[H, 3, D]`` (slot 0 = query, 1 = key, 2 = value); the query
     and key vectors of every head are rotated by ``rotate`` at the token's position, the
     value vectors are left as they are.  ``rows``: token rows to compute (default all).
+    ``bf16_steps``: round the projection to bf16 before the rotation and the result after
+    it, as a model that holds its activations in bf16 does (default: exact throughout).
     Returns fp64 ``[n_rows, H, 3, D]``.
     """
     if x_bits.shape[0] != B * S:
         raise ValueError("x must hold B*S token rows")
     y = qkv_proj(x_bits, w_bits, bias_bits, rows=rows, threads=threads).reshape(-1, H, 3, D)
+    if bf16_steps:
+        y = round_bf16(y)
     toks = np.arange(B * S, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64).reshape(-1)
     if rotary_dim:
         for n, t in enumerate(toks):
@@ -225,7 +237,7 @@ def qkv_proj_rotated(x_bits: np.ndarray, w_bits: np.ndarray, bias_bits, B: int, 
             for h in range(H):
                 for slot in (0, 1):
                     y[n, h, slot] = rotate(y[n, h, slot], pos, rotary_dim, base)
-    return y
+    return round_bf16(y) if bf16_steps else y
 
 
 def alibi_slopes(H: int) -> np.ndarray:

@@ -207,3 +207,18 @@ def test_unmodified_projection_copy_passes(tmp_path):
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_planted_projection_mistake_is_caught(tmp_path, name):
     assert not _pins_pass(_build_mutant(tmp_path, name))
+
+
+def test_bf16_steps_round_before_and_after_the_rotation():
+    B, S, H, D, r = 1, 9, 2, 32, 16
+    x, w, b = _rot_case(B, S, H, D, 12)
+    plain = oracle.qkv_proj(_bits(x), _bits(w), _bits(b)).reshape(-1, H, 3, D)
+    got = oracle.qkv_proj_rotated(_bits(x), _bits(w), _bits(b), B, S, H, D, r, bf16_steps=True)
+    y = torch.from_numpy(plain).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(got[..., 2, :], y[..., 2, :])    # values: one rounding, no rotation
+    assert np.array_equal(got[0], y[0])                    # position 0: the rotation is the identity
+    for t in (3, 8):
+        want = oracle.rotate(y[t, 1, 0], t, r, 1e4)
+        assert np.array_equal(got[t, 1, 0], torch.from_numpy(want).to(torch.bfloat16).double().numpy())
+    # every result is a bf16 value
+    assert np.array_equal(got, torch.from_numpy(got).to(torch.bfloat16).double().numpy())
