@@ -27,6 +27,10 @@ One JSON line on stdout (rank 0); everything else goes to stderr.
 
 --pass bwd times the backward (neox_attn_bwd) on a prefill workload instead: 5 B H S^2 D
 algorithmic FLOPs per step in TFLOP/s, the forward's out/lse and a seeded dout resident.
+
+--pass proj times the query_key_value projection that produces the packed qkv
+(neox_attn_qkv_proj: x[B*S, H*D] times w[H*D, 3*H*D] plus bias, query/key slots rotated
+in the epilogue): 2 M K N FLOPs per step in TFLOP/s against the same bf16 peak.
 """
 from __future__ import annotations
 
@@ -587,6 +591,172 @@ def run_bwd(args, w):
     return 0
 
 
+# ------------------------------------------------------ qkv projection ----
+PROJ_METRIC = "fused query_key_value projection (+bias, +rotary epilogue) TFLOP/s and % of B300 bf16 tensor peak"
+PROJ_KERNEL_SOURCES = ("qkv_proj.cuh", "attn_common.cuh", "ptx.cuh")
+
+
+def proj_shape(w):
+    """(M tokens, K hidden, N = 3 H D) of the workload's query_key_value projection."""
+    return w.B * w.S, w.H * w.D, 3 * w.H * w.D
+
+
+def run_proj(args, w):
+    """One step = one neox_attn_qkv_proj call: x[B*S, hidden] times w[hidden, 3 H D] plus
+    bias, the query/key slots rotated in the epilogue (rotary_dim of the workload), packed
+    qkv out.  2 M K N algorithmic FLOPs per step."""
+    import torch
+    import causal_rope_self_neox_b300 as na
+    from causal_rope_self_neox_b300.workloads import proj_inputs
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0  # one GPU: a single-replica measurement
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    M, K, N = proj_shape(w)
+    x_cpu, w_cpu, b_cpu = proj_inputs(w)
+    x, wt, b = x_cpu.to(dev), w_cpu.to(dev), b_cpu.to(dev)
+    qkv = torch.empty((w.B, w.S, w.H, 3, w.D), dtype=torch.bfloat16, device=dev)
+    flush = L2Flush(torch, dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    flops = 2.0 * M * K * N
+
+    def step(xx=x, out=qkv):
+        rc = na.neox_attn_qkv_proj(xx.data_ptr(), wt.data_ptr(), b.data_ptr(), w.B, w.S, K, w.H, w.D, w.rotary_dim,
+                                   w.rotary_base, out.data_ptr(), sh)
+        if rc != 0:
+            raise na.NeoxAttnError(rc, "neox_attn_qkv_proj")
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    na.check_device_error()
+    if not bool(torch.isfinite(qkv.float()).all()):
+        raise RuntimeError("non-finite projection after warm-up")
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = "0"
+    try:
+        u = str(props.uuid)
+        gpu_id = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        pass
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_id) as cs:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    clocks = cs.summary()
+    na.check_device_error()
+    ms = [a.elapsed_time(b_) for a, b_ in zip(starts, ends)]
+    ms_per_step = sum(ms) / len(ms)
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    # end to end: the token rows in from pinned host memory, the packed qkv back; the
+    # weight and bias stay resident, as a model's parameters do
+    hx = x_cpu.pin_memory()
+    hq = torch.empty(qkv.shape, dtype=qkv.dtype).pin_memory()
+    dx = torch.empty_like(x)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        dx.copy_(hx, non_blocking=True)
+        step(dx)
+        hq.copy_(qkv, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    na.check_device_error()
+    peak, peak_sus, hbm, src = load_peaks()
+    traffic, tsrc = profiled_traffic(w.name, "qkv_proj", PROJ_KERNEL_SOURCES)
+    line = {
+        "metric": PROJ_METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded x ~ N(0,1), w ~ N(0,1)/sqrt(hidden), bias ~ N(0,0.25), bf16)",
+        "config": {**w.describe(), "pass": "qkv_proj", "M": M, "hidden": K, "N": N, "l2": L2_NOTE},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "traffic": traffic, "traffic_source": tsrc,
+                     "peak_kind": f"{src} dense bf16 burst (cuBLAS, kernel timed alone)",
+                     "kernel": f"qkv_proj_kernel<NT={192 if w.D == 96 else 256}>",
+                     "algorithmic_flops_per_launch": flops,
+                     "algorithmic_bytes_per_launch": 2 * (M * K + K * N + N + M * N)},
+        "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+        "e2e": {"value": flops / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hq.numel() * 2, "steps": e2e_steps,
+                "ms_per_step": e2e_ms,
+                "path": "pinned host x -> device, neox_attn_qkv_proj (C ABI), qkv -> pinned host; w, bias resident"},
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": wall,
+        "kernel_ms": {"min": min(ms), "median": statistics.median(ms), "max": max(ms)},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        used = oracle.default_threads()
+        rows = list(range(min(M, 2 * used)))  # a bounded sample of token rows
+        t0 = time.perf_counter()
+        oracle.qkv_proj_rotated(bf16_bits(x_cpu), bf16_bits(w_cpu), bf16_bits(b_cpu), w.B, w.S, w.H, w.D,
+                                w.rotary_dim, w.rotary_base, rows=rows, threads=used)
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": 2.0 * len(rows) * K * N / secs / 1e12, "unit": "TFLOP/s", "cores": used,
+                                "kind": "oracle", "seconds": secs,
+                                "sample": f"{len(rows)} of the {M} token rows, fp64, {used} threads"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_proj(args, w):
+    """The projection oracle as the reference arm: each step a bounded sample of token rows."""
+    import oracle
+    from causal_rope_self_neox_b300.workloads import proj_inputs
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    threads = oracle.default_threads()
+    M, K, N = proj_shape(w)
+    x_cpu, w_cpu, b_cpu = proj_inputs(w)
+    xb, wb, bb = bf16_bits(x_cpu), bf16_bits(w_cpu), bf16_bits(b_cpu)
+    t0 = time.perf_counter()  # calibrate: one row on one thread
+    oracle.qkv_proj(xb, wb, bb, rows=[0], threads=1)
+    per_row_1t = time.perf_counter() - t0
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(M, per_step_budget / per_row_1t * threads)))
+    rows = list(range(n))
+    used = min(threads, n)
+    run = lambda: oracle.qkv_proj_rotated(xb, wb, bb, w.B, w.S, w.H, w.D, w.rotary_dim, w.rotary_base, rows=rows,
+                                          threads=used)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = 2.0 * n * K * N * args.steps / total / 1e12
+    line = {
+        "metric": PROJ_METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "pass": "qkv_proj", "M": M, "hidden": K, "N": N, "sample_rows_per_step": n,
+                   "l2": "n/a (CPU)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+                         "sample": f"{n} of {M} token rows per step, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---------------------------------------------------------- decode workloads ----
 DECODE_METRIC = "incremental decode: KV-cache GB/s read per step (and tokens/s)"
 
@@ -715,8 +885,9 @@ def main():
                     help="time the ALiBi forward (neox_attn_fwd_alibi) on the workload's shape instead")
     ap.add_argument("--rotation", choices=["auto", "fused", "pre"], default="auto",
                     help="where the forward applies the rotary embedding (neox_attn_fwd_ex placement)")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
-                    help="bwd: time the backward (neox_attn_bwd) on a prefill workload")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd", "proj"], default="fwd",
+                    help="bwd: time the backward (neox_attn_bwd) on a prefill workload; proj: the "
+                         "query_key_value projection that feeds it (neox_attn_qkv_proj)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -730,6 +901,10 @@ def main():
         if args.impl == "reference":
             return run_reference_bwd(args, w)
         return run_bwd(args, w)
+    if args.pass_ == "proj":
+        if args.impl == "reference":
+            return run_reference_proj(args, w)
+        return run_proj(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -157,16 +157,16 @@ int encode_qkv_map(CUtensorMap* map, const void* qkv, int B, int S, int H, int D
   return NEOX_OK;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] matrix, 128-byte swizzle.
-int encode_2d_sw128(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                    uint32_t box_outer) {
+// 2-D bf16 map over a row-major [outer, inner] matrix.
+int encode_2d(CUtensorMap* map, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle) {
   if (!resolve_encode()) return cuda_fail(cudaErrorNotSupported);
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return NEOX_OK;
@@ -582,9 +582,9 @@ int neox_attn_qkv_proj(const void* x, const void* w, const void* bias, int B, in
     p.num_tiles = p.num_m * ((p.N + NT - 1) / NT);
     p.wait_limit_ns = neox::kWaitLimitNs;
     CUtensorMap mx, mw, mo;
-    if ((rc = encode_2d_sw128(&mx, x, hidden, p.M, 64, 128)) != NEOX_OK) return rc;
-    if ((rc = encode_2d_sw128(&mw, w, p.N, hidden, 64, 64)) != NEOX_OK) return rc;
-    if ((rc = encode_2d_sw128(&mo, qkv, p.N, p.M, 64, 32)) != NEOX_OK) return rc;
+    if ((rc = encode_2d(&mx, x, hidden, p.M, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != NEOX_OK) return rc;
+    if ((rc = encode_2d(&mw, w, p.N, hidden, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != NEOX_OK) return rc;
+    if ((rc = encode_2d(&mo, qkv, p.N, p.M, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B)) != NEOX_OK) return rc;
     return neox::launch_qkv_proj(mx, mw, mo, p, dev.num_sms, st, &g_last_cuda_error) == 0 ? NEOX_OK : NEOX_ERR_CUDA;
   } catch (...) {
     return NEOX_ERR_CUDA;
