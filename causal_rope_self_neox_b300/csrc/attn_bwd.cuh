@@ -16,7 +16,8 @@
 //                          memory while query blocks i >= j stream through; per block
 //                          five tcgen05 MMAs (S = Q'K'^T and dP = dO V^T into TMEM, then
 //                          dV += P^T dO and dK += dS^T Q' accumulating in TMEM over i, and
-//                          dQ'_i = dS K' added to the fp32 accumulator by bulk reductions);
+//                          dQ'_i = dS K' added to the fp32 accumulator by D/32 TMA tensor
+//                          reductions of 128 x 32 boxes);
 //                          at the end dk (rotated back) and dv are written as bf16;
 //   attn_bwd_dq_kernel     rotates the accumulated dq' back and writes dq as bf16.
 // P and dS enter the MMAs as bf16 (fp32 accumulation), as do the rotated q', k' (rounded
@@ -169,12 +170,12 @@ __host__ __device__ constexpr uint32_t idesc_bwd(int M, int N, bool a_mn, bool b
 __host__ __device__ constexpr int bwd_qbufs(int D) { return D == 128 ? 1 : 2; }
 // smem: K'_j, V_j, then per buffer Q'_i and dO_i, then P_i and dS_i [128][128] tiles
 // (1 KB aligned), barriers, the TMEM address and the abort flag.
-// dq' staging for the bulk reductions: per thread D/2 floats plus 16 bytes of padding, so
-// that the slots of 8 consecutive rows start in 8 different 16-byte bank groups; it
-// reuses the P/dS tiles and, for D = 128, runs 4 KB past them.
-__host__ __device__ constexpr int bwd_stage_slot(int D) { return D / 2 * 4 + 16; }
+// dq' staging for the tensor reductions: D/32 boxes of [128 rows][32 floats] (16 KB each,
+// the TMA 128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r & 7)) in the P/dS
+// tiles, which are free once the block's dV/dK/dQ MMAs have completed.
+__host__ __device__ constexpr int bwd_stage_bytes(int D) { return D / 32 * 16384; }
 __host__ __device__ constexpr int bwd_stage_extra(int D) {
-  return 256 * bwd_stage_slot(D) > 2 * tile_bytes(128) ? 256 * bwd_stage_slot(D) - 2 * tile_bytes(128) : 0;
+  return bwd_stage_bytes(D) > 2 * tile_bytes(128) ? bwd_stage_bytes(D) - 2 * tile_bytes(128) : 0;
 }
 __host__ __device__ constexpr int bwd_smem_bytes(int D) {
   return 1024 + (2 + 2 * bwd_qbufs(D)) * tile_bytes(D) + 2 * tile_bytes(128) + bwd_stage_extra(D) + 128;
@@ -189,11 +190,14 @@ __device__ __forceinline__ uint64_t bwd_fmul2(uint64_t a, uint64_t b) {
 __device__ __forceinline__ float bwd_lo(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x)); }
 __device__ __forceinline__ float bwd_hi(uint64_t x) { return __uint_as_float(static_cast<uint32_t>(x >> 32)); }
 
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc),
-               "r"(bytes)
+// Element-wise add of a shared-memory box into the tensor at (c0, c1, c2) (fp32 per the
+// tensor map), tracked in this thread's bulk async-group; rows past the tensor's extent
+// are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* map, uint32_t ssrc, int c0, int c1, int c2) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(ssrc), "r"(c0), "r"(c1), "r"(c2)
                : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -201,7 +205,8 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
-                    const __grid_constant__ CUtensorMap tg, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tdq,
+                    const BwdParams p) {
   constexpr int NB = bwd_qbufs(D);
   constexpr int TB = tile_bytes(D);
   constexpr int DH = D / 2;  // output columns per thread
@@ -245,6 +250,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_map(&tq);
     tma_prefetch_map(&tg);
     tma_prefetch_map(&tv);
+    tma_prefetch_map(&tdq);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -394,23 +400,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) mma_pending = false;
     tc_fence_after_sync();
 
-    // ---- this thread's half of the dq' row into the fp32 accumulator: staged in the
-    //      P/dS tiles (free until the next block's P/dS), added by one bulk reduction
-    //      that runs on while the next block proceeds
-    float* stage = reinterpret_cast<float*>(Pt + (half * kRows + row) * bwd_stage_slot(D));
+    // ---- dq' of the block into the fp32 accumulator: this thread's half row staged in
+    //      the P/dS tiles (free until the next block's P/dS) as 128 x 32 boxes, then one
+    //      tensor reduction per box that runs on while the next block proceeds (query
+    //      rows past S fall outside the tensor and are skipped)
     for (int c0 = 0; c0 < DH; c0 += 16) {
       uint32_t r[16];
       tmem_ld16(tdQ + lane_off + DH * half + c0, r);
       tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 16; k += 4)
-        *reinterpret_cast<float4*>(stage + c0 + k) = make_float4(__uint_as_float(r[k]), __uint_as_float(r[k + 1]),
-                                                                 __uint_as_float(r[k + 2]), __uint_as_float(r[k + 3]));
+      for (int k = 0; k < 16; k += 4) {
+        const int col = DH * half + c0 + k;
+        *reinterpret_cast<float4*>(Pt + (col >> 5) * 16384 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4)) =
+            make_float4(__uint_as_float(r[k]), __uint_as_float(r[k + 1]), __uint_as_float(r[k + 2]),
+                        __uint_as_float(r[k + 3]));
+      }
     }
-    if (qvalid) {
-      fence_proxy_async_smem();
-      bulk_reduce_add_f32(p.dq_acc + ((static_cast<long long>(b) * p.S + q) * p.H + h) * D + DH * half,
-                          smem_u32(stage), DH * 4);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(&tdq, smem_u32(Pt + c * 16384), h * D + 32 * c, i * kRows, b);
+      bulk_commit_group();
     }
     if (NB == 1 && next) {  // single buffer: the next block's tiles only now
       fence_proxy_async_smem();

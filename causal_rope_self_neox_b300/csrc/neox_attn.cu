@@ -482,9 +482,24 @@ int encode_rows_map(CUtensorMap* map, const void* ptr, int B, int S, int H, int 
   return NEOX_OK;
 }
 
+// The fp32 dq' accumulator [B, S, H, D] as a 3-D tensor {H*D, S, B}: a box of 32 columns
+// of 128 query rows of one batch, 128-byte swizzle, for the backward's tensor reductions.
+int encode_dq_map(CUtensorMap* map, const float* ptr, int B, int S, int H, int D) {
+  if (!resolve_encode()) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(H) * D, static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * D * 4, static_cast<cuuint64_t>(S) * H * D * 4};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(neox::kRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult res = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (res != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return NEOX_OK;
+}
+
 template <int D>
 int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tg,
-               cudaStream_t stream) {
+               const CUtensorMap& tdq, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.S * p.H;
   neox::attn_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -493,7 +508,7 @@ int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMa
   e = cudaFuncSetAttribute(neox::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   const long long ctas = static_cast<long long>(p.nblk) * p.B * p.H;
-  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tv, tg, p);
+  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tv, tg, tdq, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   e = cudaGetLastError();
@@ -699,6 +714,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     if (rc != NEOX_OK) return rc;
     rc = encode_rows_map(&tg, dout, B, S, H, D);
     if (rc != NEOX_OK) return rc;
+    CUtensorMap tdq;  // the fp32 dq' accumulator at the start of the scratch
+    rc = encode_dq_map(&tdq, scratch, B, S, H, D);
+    if (rc != NEOX_OK) return rc;
     neox::BwdParams p{};
     p.qkv = static_cast<const uint16_t*>(qkv);
     p.out = static_cast<const uint16_t*>(out);
@@ -721,9 +739,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
     switch (D) {
-      case 64: return launch_bwd<64>(p, tq, tv, tg, stream);
-      case 96: return launch_bwd<96>(p, tq, tv, tg, stream);
-      default: return launch_bwd<128>(p, tq, tv, tg, stream);
+      case 64: return launch_bwd<64>(p, tq, tv, tg, tdq, stream);
+      case 96: return launch_bwd<96>(p, tq, tv, tg, tdq, stream);
+      default: return launch_bwd<128>(p, tq, tv, tg, tdq, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
