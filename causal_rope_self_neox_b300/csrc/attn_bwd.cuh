@@ -218,8 +218,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto Gb = [&](int k) { return Vt + TB + (2 * k + 1) * TB; };
   uint8_t* Pt = Vt + TB + 2 * NB * TB;
   uint8_t* St = Pt + tile_bytes(128);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(St + tile_bytes(128) + bwd_stage_extra(D));  // kv, ld[2], mma
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+  // barriers kv, ld[2], mma, rel (the block's dV and dK MMAs done), then the TMEM address
+  uint64_t* bars = reinterpret_cast<uint64_t*>(St + tile_bytes(128) + bwd_stage_extra(D));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -236,7 +237,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int j = rem / gh;
   const int bh = g0 + (rem - j * gh);
   const int b = bh / p.H, h = bh - b * p.H;
-  const uint32_t bar_kv = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[3]);
+  const uint32_t bar_kv = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[3]), bar_rel = smem_u32(&bars[4]);
   auto bar_ld = [&](int k) { return smem_u32(&bars[1 + k]); };
   const uint64_t lim = p.wait_limit_ns;
 
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_ld(0), 1);
     mbar_init(bar_ld(1), 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_rel, 1);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_map(&tq);
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // thread 0 only: copies and MMAs in flight, for the abort path
   bool kv_pending = false, mma_pending = false;
   bool ld_pending[2] = {false, false};
-  uint32_t ph_ld[2] = {0, 0}, ph_mma = 0;
+  uint32_t ph_ld[2] = {0, 0}, ph_mma = 0, ph_rel = 0;
   auto issue_qg = [&](int k, int blk) {  // Q_blk (raw) and dO_blk into buffer k
     mbar_arrive_expect_tx(bar_ld(k), 2 * TB);
     for (int cb = 0; cb < D / kBlkCols; ++cb) {
@@ -387,9 +389,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_ss(tdV, vmajor_desc(pa, kk), vmajor_desc(ga, kk), idesc_t, (i > j || kk > 0) ? 1u : 0u);
       for (int kk = 0; kk < kRows / 16; ++kk)
         mma_ss(tdK, vmajor_desc(sa, kk), vmajor_desc(qa, kk), idesc_t, (i > j || kk > 0) ? 1u : 0u);
+      // single query-side buffer: it is free once dV and dK have read dO and Q'
+      const bool early = NB == 1 && next;
+      if (early) tc_commit(bar_rel);
       for (int kc = 0; kc < kRows / 16; ++kc) mma_ss(tdQ, kmajor_desc(sa, kc), vmajor_desc(ka, kc), idesc_q, kc > 0);
       tc_commit(bar_mma);
       mma_pending = true;
+      // ... so the next block's tiles load while dQ' is computed and staged
+      if (early && wait_phase(bar_rel, ph_rel, abort_flag, lim, 46)) {
+        ph_rel ^= 1;
+        issue_qg(0, i + 1);
+      }
     }
     // the next block's tiles land while these MMAs run
     if (NB == 2 && next && !land(bi ^ 1, 44)) { ok = false; break; }
@@ -422,12 +432,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(&tdq, smem_u32(Pt + c * 16384), h * D + 32 * c, i * kRows, b);
       bulk_commit_group();
     }
-    if (NB == 1 && next) {  // single buffer: the next block's tiles only now
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (tid == 0) issue_qg(0, i + 1);
-      if (!land(0, 45)) { ok = false; break; }
-    }
+    if (NB == 1 && next && !land(0, 45)) { ok = false; break; }  // single buffer: issued above
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
