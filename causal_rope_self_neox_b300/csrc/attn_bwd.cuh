@@ -344,15 +344,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     //      reduction has read its staging area there; the barrier below covers the others)
     bulk_wait_read_all();
     __syncthreads();
-    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tS + lane_off + c0, sr);
-      tmem_ld32(tdP + lane_off + c0, dr);
-      tmem_wait_ld();
+    // both 32-column chunks of S and dP in one TMEM round trip
+    uint32_t sr2[2][32], dr2[2][32];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      tmem_ld32(tS + lane_off + 64 * half + 32 * ch, sr2[ch]);
+      tmem_ld32(tdP + lane_off + 64 * half + 32 * ch, dr2[ch]);
+    }
+    tmem_wait_ld();
+    // dS = P (dP - delta) / sqrt(D) = P * (dP / sqrt(D) - delta / sqrt(D)), in fp32 pairs
+    const uint64_t sc2 = f32x2_pack(p.scale_log2, p.scale_log2), nl2 = f32x2_pack(-lse2, -lse2);
+    const uint64_t ds2 = f32x2_pack(p.scale, p.scale), nd2 = f32x2_pack(-dl * p.scale, -dl * p.scale);
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      const int c0 = 64 * half + 32 * ch;
+      const uint32_t* sr = sr2[ch];
+      const uint32_t* dr = dr2[ch];
       uint32_t pk[16], dk[16];
-      // dS = P (dP - delta) / sqrt(D) = P * (dP / sqrt(D) - delta / sqrt(D)), in fp32 pairs
-      const uint64_t sc2 = f32x2_pack(p.scale_log2, p.scale_log2), nl2 = f32x2_pack(-lse2, -lse2);
-      const uint64_t ds2 = f32x2_pack(p.scale, p.scale), nd2 = f32x2_pack(-dl * p.scale, -dl * p.scale);
       const bool full = qvalid && static_cast<long long>(j) * kRows + c0 + 31 <= q;  // no key past the row
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
