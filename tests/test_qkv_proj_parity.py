@@ -92,6 +92,21 @@ def test_projection_on_the_neox20b_shape_sampled_rows():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("name", ["pythia160m", "pythia1.4b", "long16k"])
+def test_projection_on_the_other_workload_shapes_sampled_rows(name):
+    # D = 64 (four slots a tile, r = 16), D = 128 (r = 32), and D = 128 with every dim
+    # rotated (r = 128: the 16-byte rotation path) at 16384 tokens x hidden 4096
+    wl = WORKLOADS[name]
+    B, S, H, D, r = wl.B, wl.S, wl.H, wl.D, wl.rotary_dim
+    x, w, b = proj_inputs(wl)
+    got = _run(x, w, b, B, S, H, D, r)
+    rng = np.random.default_rng(wl.seed + 7)
+    rows = np.unique(np.concatenate([rng.choice(B * S, size=24, replace=False), [0, S - 1, B * S - 1]]))
+    ref = oracle.qkv_proj_rotated(bf16_bits(x), bf16_bits(w), bf16_bits(b), B, S, H, D, r, rows=rows)
+    _check(got[rows], ref, _bounds(x, w, b, rows, H, D, r), r)
+
+
+@pytest.mark.gpu
 def test_plain_projection_equals_rotated_one_outside_the_rotary_dims():
     # rotary_dim only touches the first r dims of the query and key slots
     B, S, hidden, H, D, r = 2, 150, 192, 2, 96, 24
