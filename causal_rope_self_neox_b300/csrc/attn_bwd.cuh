@@ -17,7 +17,9 @@
 //                          five tcgen05 MMAs (S = Q'K'^T and dP = dO V^T into TMEM, then
 //                          dV += P^T dO and dK += dS^T Q' accumulating in TMEM over i, and
 //                          dQ'_i = dS K' added to the fp32 accumulator by D/32 TMA tensor
-//                          reductions of 128 x 32 boxes);
+//                          reductions of 128 x 32 boxes, staged, with two query-side
+//                          buffers, in block i's own (then free) Q'/dO buffer and reduced
+//                          while block i+1 computes its P/dS);
 //                          at the end dk (rotated back) and dv are written as bf16;
 //   attn_bwd_dq_kernel     rotates the accumulated dq' back and writes dq as bf16.
 // P and dS enter the MMAs as bf16 (fp32 accumulation), as do the rotated q', k' (rounded
@@ -171,8 +173,9 @@ __host__ __device__ constexpr int bwd_qbufs(int D) { return D == 128 ? 1 : 2; }
 // smem: K'_j, V_j, then per buffer Q'_i and dO_i, then P_i and dS_i [128][128] tiles
 // (1 KB aligned), barriers, the TMEM address and the abort flag.
 // dq' staging for the tensor reductions: D/32 boxes of [128 rows][32 floats] (16 KB each,
-// the TMA 128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r & 7)) in the P/dS
-// tiles, which are free once the block's dV/dK/dQ MMAs have completed.
+// the TMA 128-byte swizzle: 16-byte chunk k of row r at chunk k ^ (r & 7)) in the block's
+// Q'/dO buffer (two buffers) or in the P/dS tiles (one buffer), both free once the block's
+// dV/dK/dQ MMAs have completed.
 __host__ __device__ constexpr int bwd_stage_bytes(int D) { return D / 32 * 16384; }
 __host__ __device__ constexpr int bwd_stage_extra(int D) {
   return bwd_stage_bytes(D) > 2 * tile_bytes(128) ? bwd_stage_bytes(D) - 2 * tile_bytes(128) : 0;
@@ -299,6 +302,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     kv_pending = true;
     issue_qg(0, j);
+    if (NB == 2 && j + 1 < p.nblk) issue_qg(1, j + 1);
   }
   wait_phase(bar_kv, 0, abort_flag, lim, 42);
   __syncthreads();
@@ -316,10 +320,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   for (int i = j; i < p.nblk && ok; ++i) {
     const int bi = NB == 2 ? ((i - j) & 1) : 0;
     const bool next = i + 1 < p.nblk;
-    // ---- next block's tiles into the other buffer (free: block i-1 is done), then
-    //      S = Q' K'^T and dP = dO V^T
+    // ---- S = Q' K'^T and dP = dO V^T
     if (tid == 0) {
-      if (NB == 2 && next) issue_qg(bi ^ 1, i + 1);
       tc_fence_after_sync();
       const uint32_t qa = smem_u32(Qb(bi)), ka = smem_u32(Kt), ga = smem_u32(Gb(bi)), va = smem_u32(Vt);
       for (int kc = 0; kc < D / 16; ++kc) mma_ss(tS, kmajor_desc(qa, kc), kmajor_desc(ka, kc), idesc_s, kc > 0);
@@ -339,11 +341,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) mma_pending = false;
     tc_fence_after_sync();
 
+    // ---- the previous block's dq' reductions run under this block's P/dS (two buffers:
+    //      staged in that block's Q'/dO buffer); with one buffer they were staged in the
+    //      P/dS tiles, which must have been read before P/dS overwrite them
+    if (NB == 2) {
+      if (tid == 0 && i > j) {
+        for (int c = 0; c < D / 32; ++c)
+          tma_reduce_add_3d(&tdq, smem_u32(Qb(bi ^ 1) + c * 16384), h * D + 32 * c, (i - 1) * kRows, b);
+        bulk_commit_group();
+      }
+    } else {
+      bulk_wait_read_all();
+      __syncthreads();
+    }
     // ---- P = exp(S/sqrt(D) - lse), dS = P (dP - delta) / sqrt(D) for this thread's 64
-    //      keys of the row, to shared memory as bf16 (once this thread's previous dq'
-    //      reduction has read its staging area there; the barrier below covers the others)
-    bulk_wait_read_all();
-    __syncthreads();
+    //      keys of the row, to shared memory as bf16
     // both 32-column chunks of S and dP in one TMEM round trip
     uint32_t sr2[2][32], dr2[2][32];
 #pragma unroll
@@ -408,9 +420,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ph_rel ^= 1;
         issue_qg(0, i + 1);
       }
+      // two buffers: the other one, once the previous block's reductions have read its
+      // staging, takes the next block's tiles (the first block's were loaded up front)
+      if (NB == 2 && next && i > j) {
+        bulk_wait_read_all();
+        issue_qg(bi ^ 1, i + 1);
+      }
     }
-    // the next block's tiles land while these MMAs run
-    if (NB == 2 && next && !land(bi ^ 1, 44)) { ok = false; break; }
     wait_phase(bar_mma, ph_mma, abort_flag, lim, 41);
     __syncthreads();
     if (*abort_flag) { ok = false; break; }
@@ -418,10 +434,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) mma_pending = false;
     tc_fence_after_sync();
 
-    // ---- dq' of the block into the fp32 accumulator: this thread's half row staged in
-    //      the P/dS tiles (free until the next block's P/dS) as 128 x 32 boxes, then one
-    //      tensor reduction per box that runs on while the next block proceeds (query
-    //      rows past S fall outside the tensor and are skipped)
+    // ---- dq' of the block into the fp32 accumulator: this thread's half row staged as
+    //      128 x 32 boxes, then one tensor reduction per box that runs on while the next
+    //      block proceeds (query rows past S fall outside the tensor and are skipped)
+    uint8_t* stg = NB == 2 ? Qb(bi) : Pt;
     for (int c0 = 0; c0 < DH; c0 += 16) {
       uint32_t r[16];
       tmem_ld16(tdQ + lane_off + DH * half + c0, r);
@@ -429,18 +445,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int k = 0; k < 16; k += 4) {
         const int col = DH * half + c0 + k;
-        *reinterpret_cast<float4*>(Pt + (col >> 5) * 16384 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4)) =
+        *reinterpret_cast<float4*>(stg + (col >> 5) * 16384 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4)) =
             make_float4(__uint_as_float(r[k]), __uint_as_float(r[k + 1]), __uint_as_float(r[k + 2]),
                         __uint_as_float(r[k + 3]));
       }
     }
     fence_proxy_async_smem();
     __syncthreads();
-    if (tid == 0) {
-      for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(&tdq, smem_u32(Pt + c * 16384), h * D + 32 * c, i * kRows, b);
+    // one buffer: reduce now; two: at the next block's P/dS (or now, after the last block)
+    if (tid == 0 && (NB == 1 || !next)) {
+      for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(&tdq, smem_u32(stg + c * 16384), h * D + 32 * c, i * kRows, b);
       bulk_commit_group();
     }
     if (NB == 1 && next && !land(0, 45)) { ok = false; break; }  // single buffer: issued above
+    if (NB == 2 && next && !land(bi ^ 1, 44)) { ok = false; break; }
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
