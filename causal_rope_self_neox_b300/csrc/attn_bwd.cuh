@@ -402,6 +402,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     // ---- dV += P^T dO, dK += dS^T Q' (accumulating over i), dQ'_i = dS K'
     if (tid == 0) {
+      // two buffers: the other one, whose staging the previous block's reductions have read
+      // by now, takes the next block's tiles first, so they load under these MMAs (the
+      // first block's were loaded up front)
+      if (NB == 2 && next && i > j) {
+        bulk_wait_read_all();
+        issue_qg(bi ^ 1, i + 1);
+      }
       tc_fence_after_sync();
       const uint32_t pa = smem_u32(Pt), sa = smem_u32(St), ga = smem_u32(Gb(bi)), qa = smem_u32(Qb(bi)),
                      ka = smem_u32(Kt);
@@ -419,12 +426,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (early && wait_phase(bar_rel, ph_rel, abort_flag, lim, 46)) {
         ph_rel ^= 1;
         issue_qg(0, i + 1);
-      }
-      // two buffers: the other one, once the previous block's reductions have read its
-      // staging, takes the next block's tiles (the first block's were loaded up front)
-      if (NB == 2 && next && i > j) {
-        bulk_wait_read_all();
-        issue_qg(bi ^ 1, i + 1);
       }
     }
     wait_phase(bar_mma, ph_mma, abort_flag, lim, 41);
