@@ -56,6 +56,7 @@ def check(got, ref, what):
     (1, 1, 2, 64, 16),       # one token: dq = dk = 0, dv = dout
     (1, 384, 1, 96, 6),      # rotary_dim not a multiple of 8
     (1, 1000, 1, 128, 32),
+    (1, 700, 2, 96, 24),     # six key blocks, ragged: both query-side buffers cycle (dq' staged in them)
 ])
 def test_bwd_small_shapes(B, S, H, D, r):
     qkv = make_qkv(B, S, H, D, seed=S + D + r)
