@@ -285,36 +285,42 @@ __global__ void __launch_bounds__(kProjThreads, 1)
         // the slab's previous stores have read it
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
+        // two 32-column chunks per TMEM round trip (their bias words fetched meanwhile)
 #pragma unroll 1
-        for (int c = 0; c < NB; ++c) {
-          uint32_t v[32];
-          tmem_ld32(taddr + static_cast<uint32_t>(h0 + 32 * c), v);
-          float bias[32];
-          const int n = n0 + h0 + 32 * c;
-          if (p.bias != nullptr && n < p.N) {
-            const uint4* bp = reinterpret_cast<const uint4*>(p.bias + n);
+        for (int c2 = 0; c2 < NB; c2 += 2) {
+          const int nc = NB - c2 < 2 ? NB - c2 : 2;
+          uint32_t v[2][32];
+          uint4 bw[2][4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint4 w = __ldg(bp + u);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          for (int k = 0; k < 2; ++k) {
+            if (k < nc) tmem_ld32(taddr + static_cast<uint32_t>(h0 + 32 * (c2 + k)), v[k]);
+            const int n = n0 + h0 + 32 * (c2 + k);
+            const bool has_bias = k < nc && p.bias != nullptr && n < p.N;
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                bias[8 * u + 2 * e] = __uint_as_float(ws[e] << 16);
-                bias[8 * u + 2 * e + 1] = __uint_as_float(ws[e] & 0xFFFF0000u);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) bias[e] = 0.0f;
+            for (int u = 0; u < 4; ++u)
+              bw[k][u] = has_bias ? __ldg(reinterpret_cast<const uint4*>(p.bias + n) + u) : make_uint4(0, 0, 0, 0);
           }
           tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(v[2 * e]) + bias[2 * e], __uint_as_float(v[2 * e + 1]) + bias[2 * e + 1]);
+          for (int k = 0; k < 2; ++k) {
+            if (k >= nc) break;
+            const int c = c2 + k;
+            uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_shared_v4(slab_chunk(slab, lane, 32 * c + 8 * u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t ws[4] = {bw[k][u].x, bw[k][u].y, bw[k][u].z, bw[k][u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int q2 = 4 * u + e;  // packed pair index: columns 2 q2, 2 q2 + 1
+                pk[q2] = pack_bf16x2(__uint_as_float(v[k][2 * q2]) + __uint_as_float(ws[e] << 16),
+                                     __uint_as_float(v[k][2 * q2 + 1]) + __uint_as_float(ws[e] & 0xFFFF0000u));
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(slab_chunk(slab, lane, 32 * c + 8 * u), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                           pk[4 * u + 3]);
+          }
         }
         if (half == 1) {
           // the accumulator is read: hand it back to the MMA warp
