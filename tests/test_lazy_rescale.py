@@ -1,0 +1,105 @@
+"""GPU parity of the lazy rescale path (the correction warps) against the oracle.
+
+With unit-normal inputs a row's running max settles within the first key block, so the
+forward kernel's lazy correction (rescale O only when the max grew by more than 2^8) never
+runs.  These inputs force it: key block b is scaled by 2^b, so the scores of a row roughly
+double from one block to the next, and the odd query rows are scaled by 2^-6, so their
+scores stay small and they never rescale (warps whose rows mix both cases).  Every scale
+is a power of two, exact in bf16.  Each test first checks on the host, from the oracle's
+own rotated vectors in fp64, that the inputs do produce such events, then compares every
+row with the oracle at the forward tolerances.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from causal_rope_self_neox_b300.workloads import bf16_bits, make_qkv
+
+OUT_MAX, OUT_RMS, LSE_MAX = 2e-2, 3e-3, 1e-3
+LOG2E = 1.4426950408889634
+
+
+def growing_keys_qkv(B, S, H, D, seed):
+    x = make_qkv(B, S, H, D, seed).float()
+    for b in range((S + 127) // 128):
+        x[:, 128 * b:128 * (b + 1), :, 1, :] *= 2.0 ** b
+    x[:, 1::2, :, 0, :] *= 2.0 ** -6
+    return x.to(torch.bfloat16)
+
+
+def rescale_events(qkv, B, S, H, D, r, slopes=None):
+    """Per (b, h, row): how often the running max (log2 units, scale log2(e)/sqrt(D)) grows
+    by more than 8 at a later 128-key block, from fp64 rotated scores."""
+    x = qkv.float().double().numpy()
+    ev = np.zeros((B, H, S), dtype=np.int64)
+    for b in range(B):
+        for h in range(H):
+            q = np.stack([oracle.rotate(x[b, i, h, 0], i, r, 1e4) for i in range(S)]) if r else x[b, :, h, 0]
+            k = np.stack([oracle.rotate(x[b, i, h, 1], i, r, 1e4) for i in range(S)]) if r else x[b, :, h, 1]
+            s = (q @ k.T) / np.sqrt(D)
+            if slopes is not None:
+                s = s - slopes[h] * (np.arange(S)[:, None] - np.arange(S)[None, :])
+            s = s * LOG2E
+            s[np.triu_indices(S, 1)] = -np.inf
+            for i in range(S):
+                m = None
+                for j in range(i // 128 + 1):
+                    bm = s[i, 128 * j:128 * (j + 1)].max()
+                    if m is None:
+                        m = bm
+                    elif bm > m + 8.0:
+                        ev[b, h, i] += 1
+                        m = bm
+    return ev
+
+
+def check(out, lse, ref_out, ref_lse, what):
+    e = out.float().cpu().numpy().astype(np.float64) - ref_out
+    l = lse.cpu().numpy().astype(np.float64) - ref_lse
+    assert np.isfinite(e).all() and np.isfinite(l).all(), what
+    omax, orms, lmax = np.abs(e).max(), np.sqrt((e ** 2).mean()), np.abs(l).max()
+    assert omax <= OUT_MAX and orms <= OUT_RMS and lmax <= LSE_MAX, (what, omax, orms, lmax)
+
+
+def assert_premise(ev, odd_rows_quiet=True):
+    # most even rows past the first key block rescale (several times in the later tiles);
+    # without ALiBi the odd rows never do (with it, the distance bias alone lifts a row's
+    # max from one block to the next)
+    even = ev[:, :, 128::2]
+    assert (even > 0).mean() > 0.5, (even > 0).mean()
+    assert even.max() >= 2
+    if odd_rows_quiet:
+        assert ev[:, :, 1::2].sum() == 0
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("B,S,H,D,r", [
+    (1, 600, 2, 64, 16),    # ragged last tile
+    (1, 600, 2, 96, 24),    # the packed r = 24 cross terms
+    (2, 520, 1, 128, 32),   # two sequences, a query unit with tile 1 only partly filled
+    (1, 600, 2, 128, 128),  # every dim rotated: the pre-rotated operands
+    (1, 640, 2, 96, 0),     # no rotation, whole tiles
+])
+def test_lazy_rescale_matches_oracle_on_every_row(B, S, H, D, r):
+    import causal_rope_self_neox_b300 as na
+    qkv = growing_keys_qkv(B, S, H, D, seed=S + D + r)
+    assert_premise(rescale_events(qkv, B, S, H, D, r))
+    out, lse = na.attn_fwd(qkv.cuda(), r)
+    torch.cuda.synchronize()
+    na.check_device_error()
+    ref_out, ref_lse = oracle.fwd(bf16_bits(qkv), B, S, H, D, r, 1e4)
+    check(out, lse, ref_out, ref_lse, f"B{B} S{S} H{H} D{D} r{r}")
+
+
+@pytest.mark.gpu
+def test_lazy_rescale_with_alibi_matches_oracle_on_every_row():
+    import causal_rope_self_neox_b300 as na
+    B, S, H, D = 1, 600, 3, 96
+    qkv = growing_keys_qkv(B, S, H, D, seed=123)
+    assert_premise(rescale_events(qkv, B, S, H, D, 0, slopes=oracle.alibi_slopes(H)), odd_rows_quiet=False)
+    out, lse = na.attn_fwd_alibi(qkv.cuda())
+    torch.cuda.synchronize()
+    na.check_device_error()
+    ref_out, ref_lse = oracle.fwd_alibi(bf16_bits(qkv), B, S, H, D)
+    check(out, lse, ref_out, ref_lse, "alibi")
