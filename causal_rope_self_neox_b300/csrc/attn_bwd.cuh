@@ -183,7 +183,7 @@ __host__ __device__ constexpr int bwd_stage_extra(int D) {
 __host__ __device__ constexpr int bwd_smem_bytes(int D) {
   return 1024 + (2 + 2 * bwd_qbufs(D)) * tile_bytes(D) + 2 * tile_bytes(128) + bwd_stage_extra(D) + 128;
 }
-constexpr int kBwdThreads = 256;  // two threads per tile row (each half of the columns)
+constexpr int kBwdThreads = 512;  // four threads per tile row (each a quarter of the columns)
 
 __device__ __forceinline__ uint64_t bwd_fmul2(uint64_t a, uint64_t b) {
   uint64_t r;
@@ -212,7 +212,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const BwdParams p) {
   constexpr int NB = bwd_qbufs(D);
   constexpr int TB = tile_bytes(D);
-  constexpr int DH = D / 2;  // output columns per thread
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* Kt = smem;
@@ -227,7 +226,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int row = tid & (kRows - 1), half = tid >> 7;
+  const int row = tid & (kRows - 1), part = tid >> 7;  // tile row, quarter of the row
   // CTA order: heads in groups of heads_per_group (their Q'/dO tiles, read by every key
   // block of a head, stay in L2 while the group runs); inside a group the heaviest key
   // blocks (j = 0, every query block) come first
@@ -354,22 +353,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bulk_wait_read_all();
       __syncthreads();
     }
-    // ---- P = exp(S/sqrt(D) - lse), dS = P (dP - delta) / sqrt(D) for this thread's 64
+    // ---- P = exp(S/sqrt(D) - lse), dS = P (dP - delta) / sqrt(D) for this thread's 32
     //      keys of the row, to shared memory as bf16
-    // both 32-column chunks of S and dP in one TMEM round trip
-    uint32_t sr2[2][32], dr2[2][32];
-#pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-      tmem_ld32(tS + lane_off + 64 * half + 32 * ch, sr2[ch]);
-      tmem_ld32(tdP + lane_off + 64 * half + 32 * ch, dr2[ch]);
-    }
+    uint32_t sr2[1][32], dr2[1][32];
+    tmem_ld32(tS + lane_off + 32 * part, sr2[0]);
+    tmem_ld32(tdP + lane_off + 32 * part, dr2[0]);
     tmem_wait_ld();
     // dS = P (dP - delta) / sqrt(D) = P * (dP / sqrt(D) - delta / sqrt(D)), in fp32 pairs
     const uint64_t sc2 = f32x2_pack(p.scale_log2, p.scale_log2), nl2 = f32x2_pack(-lse2, -lse2);
     const uint64_t ds2 = f32x2_pack(p.scale, p.scale), nd2 = f32x2_pack(-dl * p.scale, -dl * p.scale);
 #pragma unroll
-    for (int ch = 0; ch < 2; ++ch) {
-      const int c0 = 64 * half + 32 * ch;
+    for (int ch = 0; ch < 1; ++ch) {
+      const int c0 = 32 * part;
       const uint32_t* sr = sr2[ch];
       const uint32_t* dr = dr2[ch];
       uint32_t pk[16], dk[16];
@@ -435,17 +430,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) mma_pending = false;
     tc_fence_after_sync();
 
-    // ---- dq' of the block into the fp32 accumulator: this thread's half row staged as
+    // ---- dq' of the block into the fp32 accumulator: this thread's 16-column chunks staged as
     //      128 x 32 boxes, then one tensor reduction per box that runs on while the next
     //      block proceeds (query rows past S fall outside the tensor and are skipped)
     uint8_t* stg = NB == 2 ? Qb(bi) : Pt;
-    for (int c0 = 0; c0 < DH; c0 += 16) {
+    for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
-      tmem_ld16(tdQ + lane_off + DH * half + c0, r);
+      tmem_ld16(tdQ + lane_off + c0, r);
       tmem_wait_ld();
 #pragma unroll
       for (int k = 0; k < 16; k += 4) {
-        const int col = DH * half + c0 + k;
+        const int col = c0 + k;
         *reinterpret_cast<float4*>(stg + (col >> 5) * 16384 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4)) =
             make_float4(__uint_as_float(r[k]), __uint_as_float(r[k + 1]), __uint_as_float(r[k + 2]),
                         __uint_as_float(r[k + 3]));
@@ -473,9 +468,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool kvalid = key < p.S;
     uint16_t* dst = p.dqkv + ((static_cast<long long>(b) * p.S + (kvalid ? key : 0)) * p.H + h) * 3 * D;
     // dk' rows staged in shared memory (the query-side tiles are free now), padded rows,
-    // so the rotation can read the pair partners of the other half
+    // so the rotation can read the pair partners held by the row's other threads
     float* xs = reinterpret_cast<float*>(Qb(0)) + row * (D + 1);
-    for (int c0 = DH * half; c0 < DH * half + DH; c0 += 16) {
+    for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
       tmem_ld16(tdK + lane_off + c0, r);
       tmem_wait_ld();
@@ -485,7 +480,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     const int h2 = p.r >> 1;
     if (kvalid) {
-      for (int d0 = DH * half; d0 < DH * half + DH; d0 += 8) {
+      for (int d0 = 8 * part; d0 < D; d0 += 32) {
         float y[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -504,7 +499,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                              pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
       }
     }
-    for (int c0 = DH * half; c0 < DH * half + DH; c0 += 16) {
+    for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
       tmem_ld16(tdV + lane_off + c0, r);
       tmem_wait_ld();
