@@ -460,16 +460,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
   }
 
-  // ---- dk = R(key)^T dk' and dv for the rows of key block j, bf16 into slots 1 and 2
-  bulk_wait_read_all();
-  __syncthreads();
+  // ---- dk = R(key)^T dk' and dv for the rows of key block j, bf16 into slots 1 and 2.
+  // dk' is staged in shared memory (padded rows, so the rotation can read the pair partners
+  // held by the row's other threads): with two query-side buffers in the P/dS tiles (the
+  // last block's dq' reduction reads that block's own Q'/dO buffer), with one in the
+  // query-side tiles once that reduction has read them.
+  if (NB == 1) {
+    bulk_wait_read_all();
+    __syncthreads();
+  }
   if (ok && !*abort_flag) {
     tc_fence_after_sync();
     const bool kvalid = key < p.S;
+    const int h2 = p.r >> 1;
     uint16_t* dst = p.dqkv + ((static_cast<long long>(b) * p.S + (kvalid ? key : 0)) * p.H + h) * 3 * D;
-    // dk' rows staged in shared memory (the query-side tiles are free now), padded rows,
-    // so the rotation can read the pair partners held by the row's other threads
-    float* xs = reinterpret_cast<float*>(Qb(0)) + row * (D + 1);
+    // the table entries of this thread's first 8-dim group, requested before the staging
+    float2 cs0[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int d = 8 * part + e;
+      cs0[e] = kvalid && d < p.r ? p.cs[key * h2 + (d < h2 ? d : d - h2)] : make_float2(1.0f, 0.0f);
+    }
+    float* xs = reinterpret_cast<float*>(NB == 2 ? Pt : Qb(0)) + row * (D + 1);
     for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
       tmem_ld16(tdK + lane_off + c0, r);
@@ -477,28 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int k = 0; k < 16; ++k) xs[c0 + k] = __uint_as_float(r[k]);
     }
-    __syncthreads();
-    const int h2 = p.r >> 1;
-    if (kvalid) {
-      for (int d0 = 8 * part; d0 < D; d0 += 32) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int d = d0 + e;
-          float v = xs[d];
-          if (d < h2) {
-            const float2 c = p.cs[key * h2 + d];
-            v = fmaf(v, c.x, xs[d + h2] * c.y);
-          } else if (d < p.r) {
-            const float2 c = p.cs[key * h2 + (d - h2)];
-            v = fmaf(v, c.x, -xs[d - h2] * c.y);
-          }
-          y[e] = v;
-        }
-        *reinterpret_cast<uint4*>(dst + D + d0) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                             pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-      }
-    }
+    // dv needs no partner: written while the other threads finish staging dk'
     for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
       tmem_ld16(tdV + lane_off + c0, r);
@@ -511,6 +502,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
                          pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
                          pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
+      }
+    }
+    __syncthreads();
+    if (kvalid) {
+      for (int d0 = 8 * part; d0 < D; d0 += 32) {
+        const bool first = d0 == 8 * part;
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int d = d0 + e;
+          float v = xs[d];
+          if (d < h2) {
+            const float2 c = first ? cs0[e] : p.cs[key * h2 + d];
+            v = fmaf(v, c.x, xs[d + h2] * c.y);
+          } else if (d < p.r) {
+            const float2 c = first ? cs0[e] : p.cs[key * h2 + (d - h2)];
+            v = fmaf(v, c.x, -xs[d - h2] * c.y);
+          }
+          y[e] = v;
+        }
+        *reinterpret_cast<uint4*>(dst + D + d0) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                             pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
       }
     }
   }
