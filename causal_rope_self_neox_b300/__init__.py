@@ -24,6 +24,7 @@ NEOX_ERR_DEVICE_TIMEOUT = -5
 NEOX_ERR_NO_DEVICE_SUPPORT = -6
 NEOX_ERR_TOO_LARGE = -7
 NEOX_ERR_DEVICE_BAD_POSITION = -8
+NEOX_ERR_DEVICE_RANGE = -9
 
 NEOX_ROTATION_AUTO = 0
 NEOX_ROTATION_FUSED = 1

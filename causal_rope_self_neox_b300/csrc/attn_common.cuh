@@ -12,10 +12,12 @@
 namespace neox {
 
 // Error word (per device).  Bit 0: a bounded wait ran out; bit 1: a device-side input
-// check failed.  Bits 8..15: the site.
+// check failed; bit 2: a rotated query/key value did not fit its fp16 operand.  Bits
+// 8..15: the site.
 __device__ unsigned int g_device_error = 0;
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrBadInput = 2u;  // an input read on the device was out of range
+constexpr unsigned int kErrRange = 4u;     // |rotated q or k| > 65504 where fp16 operands are used
 
 // A wait that has not completed after this long is treated as a hang: the kernel records
 // it, stops its own work and exits cleanly instead of blocking the GPU.

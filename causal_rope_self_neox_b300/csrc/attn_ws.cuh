@@ -65,6 +65,13 @@ __host__ __device__ constexpr int rot_kind(int r) {
 }
 // float4 table entries per row loaded ahead of a tile's data.
 __host__ __device__ constexpr int rot_ahead(int rk) { return rk == kRotR16 ? 4 : rk == kRotR24 ? 6 : rk == kRotR32 ? 8 : 0; }
+// In-kernel rotation with fp16 operands for the rotated chunks (rotary_dim 16, 24, 32): the
+// first rot_f16_chunks 16-column chunks of Q' and K' are fp16, the S MMA has no lo products.
+// The other rotary_dims (and pre-rotated operands) keep the bf16 hi/lo split.
+__host__ __device__ constexpr bool rot_f16(int rk, bool pre) {
+  return !pre && (rk == kRotR16 || rk == kRotR24 || rk == kRotR32);
+}
+__host__ __device__ constexpr int rot_f16_chunks(int rk) { return rk == kRotR16 ? 1 : 2; }
 
 // Shared-memory carve-up, identical on host and device: the two query tiles (each followed
 // by its side tile), the K ring (each slot a tile and its side tile), the V ring, then the
@@ -313,6 +320,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     {
       const uint32_t lead = elect_lane();
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, false);
+      const uint32_t idesc_s16 = idesc_f16_f32(128, 128, false);  // fp16 chunks (rot_f16)
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, true);
       // Every operand buffer sits at a fixed shared address for the whole kernel, so each
       // descriptor is a base below plus a constant: the issue loop is adds and MMAs only.
@@ -375,6 +383,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 tc_fence_after_sync();
               }
               const uint64_t q = dq[tau], qs = dqs[tau];
+              if constexpr (rot_f16(RK, PRE)) {
+                // the rotated chunks as fp16 x fp16, the rest bf16 x bf16, one accumulator
+                constexpr int NF = rot_f16_chunks(RK);
+                mma_ss_l(lead, tS, qd[tau][0], kd[0], idesc_s16, 0);
+#pragma unroll
+                for (int kc = 1; kc < D / 16; ++kc)
+                  mma_ss_acc_l(lead, tS, qd[tau][kc], kd[kc], kc < NF ? idesc_s16 : idesc_s);
+              } else {
               mma_ss_l(lead, tS, qd[tau][0], kd[0], idesc_s, 0);
 #pragma unroll
               for (int kc = 1; kc < D / 16; ++kc) mma_ss_acc_l(lead, tS, qd[tau][kc], kd[kc], idesc_s);
@@ -391,6 +407,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                   mma_ss_acc_l(lead, tS, qs + kchunk_off(kc), dk + kchunk_off(kc), idesc_s);
                   mma_ss_acc_l(lead, tS, q + kchunk_off(kc), dks + kchunk_off(kc), idesc_s);
                 }
+              }
               }
               issued = true;
               tc_commit_l(lead, bar(BAR_S_FULL + tau));
@@ -460,15 +477,18 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         uint8_t* side = smem + (isq ? L.q_side(qt) : L.k_side(s));
         if (PRE) {
           // operands arrive rotated: only hand them on
-        } else if (RK == kRotR24) {  // packed cross terms of dims 16..23 (see the MMA issue)
-          rotate_row_small<3>(tile, side, tt, ta0, isq ? 1 : 2);
-          rotate_row_small<3>(tile, side, tt + 64, ta1, isq ? 1 : 2);
-        } else if (RK == kRotR16 || RK == kRotR32) {
+        } else if (RK == kRotR24) {  // fp16 chunks 0 and 1 (see rot_f16)
+          const bool in0 = rotate_row_r24_f16(tile, tt, ta0);
+          const bool in1 = rotate_row_r24_f16(tile, tt + 64, ta1);
+          if (!(in0 && in1)) record_error(kErrRange, 23);
+        } else if (RK == kRotR16 || RK == kRotR32) {  // fp16 chunk(s) 0 (and 1)
+          bool in = true;
 #pragma unroll
           for (int g = 0; g < AH / 4; ++g) {
-            rotate_group8(tile, side, tt, 8 * g, h, ta0 + 4 * g);
-            rotate_group8(tile, side, tt + 64, 8 * g, h, ta1 + 4 * g);
+            in &= rotate_group8_f16(tile, tt, 8 * g, h, ta0 + 4 * g);
+            in &= rotate_group8_f16(tile, tt + 64, 8 * g, h, ta1 + 4 * g);
           }
+          if (!in) record_error(kErrRange, 23);
         } else if (RK == kRotGroups) {
           rotate_two_rows_groups(tile, side, tt, tt + 64, pos_of(blk, tt), pos_of(blk, tt + 64), p.cs, h, ta0, ta1);
         } else if (RK == kRotScalar) {

@@ -757,7 +757,8 @@ int neox_attn_get_device_error(void) {
   e = cudaMemcpyToSymbol(neox::g_device_error, &zero, sizeof zero);
   if (e != cudaSuccess) return cuda_fail(e);
   if (v & neox::kErrTimeout) reset_decode_counters();
-  return (v & neox::kErrTimeout) ? NEOX_ERR_DEVICE_TIMEOUT : NEOX_ERR_DEVICE_BAD_POSITION;
+  if (v & neox::kErrTimeout) return NEOX_ERR_DEVICE_TIMEOUT;
+  return (v & neox::kErrRange) ? NEOX_ERR_DEVICE_RANGE : NEOX_ERR_DEVICE_BAD_POSITION;
 }
 
 const char* neox_attn_status_string(int status) {
@@ -771,6 +772,7 @@ const char* neox_attn_status_string(int status) {
     case NEOX_ERR_NO_DEVICE_SUPPORT: return "device is not compute capability 10.3";
     case NEOX_ERR_TOO_LARGE: return "S * rotary_dim/2 exceeds the fixed 1048576-entry table of neox_attn_fwd_noalloc";
     case NEOX_ERR_DEVICE_BAD_POSITION: return "a decode position was outside [0, Smax)";
+    case NEOX_ERR_DEVICE_RANGE: return "a rotated query/key value exceeded the fp16 operand range (65504)";
     default: return "unknown status";
   }
 }

@@ -266,6 +266,56 @@ __device__ __forceinline__ void rotate_group8(uint8_t* __restrict__ tile, uint8_
   *reinterpret_cast<uint4*>(side + sw64_off(row, i0 + h)) = lo;
 }
 
+// ---- fp16 operands for the rotated chunks (rotary_dim 16, 24, 32, in-kernel rotation) ----
+// The rotated values, and for rotary_dim 24 dims 24..31 as they are, are rounded once to fp16
+// in place, so the first rotary_dim/16 (rounded up) 16-column MMA chunks run as fp16 x fp16
+// (the others bf16 x bf16) with no lo products: fp16 keeps 11 significant bits to bf16's 8.
+// fp16 holds |v| <= 65504; each call returns false when a value it wrote is beyond that.
+__device__ __forceinline__ uint4 pack8_f16(const float* v) {
+  return make_uint4(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]), pack_f16x2(v[4], v[5]), pack_f16x2(v[6], v[7]));
+}
+__device__ __forceinline__ float absmax8(const float* v) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+constexpr float kF16Max = 65504.0f;
+
+// rotary_dim 24: dims 0..23 rotated and 24..31 unchanged, as fp16 (MMA chunks 0 and 1).
+__device__ __forceinline__ bool rotate_row_r24_f16(uint8_t* __restrict__ tile, int row, const float4* t) {
+  float x[32], y[24];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, 8 * c)), x + 8 * c);
+#pragma unroll
+  for (int i = 0; i < 12; ++i) {  // the expressions of rotate_row_small
+    const float cth = (i & 1) ? t[i >> 1].z : t[i >> 1].x;
+    const float sth = (i & 1) ? t[i >> 1].w : t[i >> 1].y;
+    y[i] = fmaf(x[i], cth, -x[i + 12] * sth);
+    y[i + 12] = fmaf(x[i + 12], cth, x[i] * sth);
+  }
+  float m = absmax8(x + 24);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float* v = c < 3 ? y + 8 * c : x + 24;
+    if (c < 3) m = fmaxf(m, absmax8(v));
+    *reinterpret_cast<uint4*>(tile + sw64_off(row, 8 * c)) = pack8_f16(v);
+  }
+  return !(m > kF16Max);
+}
+
+// r % 16 == 0 (16 or 32): eight pairs (i0..i0+7 with partners i0+h..i0+h+7), as fp16.
+__device__ __forceinline__ bool rotate_group8_f16(uint8_t* __restrict__ tile, int row, int i0, int h,
+                                                  const float4* t) {
+  float x[8], z[8], y[8], w[8];
+  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0)), x);
+  unpack8(*reinterpret_cast<const uint4*>(tile + sw64_off(row, i0 + h)), z);
+  rotate_pairs8(x, z, t, y, w);
+  *reinterpret_cast<uint4*>(tile + sw64_off(row, i0)) = pack8_f16(y);
+  *reinterpret_cast<uint4*>(tile + sw64_off(row, i0 + h)) = pack8_f16(w);
+  return !(fmaxf(absmax8(y), absmax8(w)) > kF16Max);
+}
+
 // Two rows of a tile for r % 16 == 0, any size: group g's table loads are issued while
 // group g-1 is being rotated.  t0 / t1 (8 float4 each) are the caller's buffers for
 // rows row0 / row1: entries [0, 4) and [4, 8) alternate between groups.

@@ -46,7 +46,8 @@ typedef enum {
   NEOX_ERR_DEVICE_TIMEOUT = -5,       /* a kernel's bounded wait ran out; results are not valid */
   NEOX_ERR_NO_DEVICE_SUPPORT = -6,    /* current device is not compute capability 10.3 (B300) */
   NEOX_ERR_TOO_LARGE = -7,            /* neox_attn_fwd_noalloc: S * rotary_dim/2 > 1048576 */
-  NEOX_ERR_DEVICE_BAD_POSITION = -8   /* neox_attn_decode: a pos[b] was outside [0, Smax) */
+  NEOX_ERR_DEVICE_BAD_POSITION = -8,  /* neox_attn_decode: a pos[b] was outside [0, Smax) */
+  NEOX_ERR_DEVICE_RANGE = -9          /* forward: a rotated q/k value exceeded 65504 (see neox_attn_fwd) */
 } neox_status;
 
 /*
@@ -72,16 +73,28 @@ typedef enum {
  * the rotation is placed in a separate pass (see neox_attn_fwd_ex), the rotated copy
  * lives in the library's per-device scratch.
  *
+ * Numerics: scores and outputs accumulate in fp32.  The rotated dims of Q and K are
+ * computed in fp32 and enter the score MMA rounded once to fp16 when the rotation runs in
+ * the attention kernel at rotary_dim 16, 24 or 32 (those 16-column chunks, including dims
+ * 24..31 at rotary_dim 24, are fp16 x fp16, the rest bf16 x bf16); at any other
+ * rotary_dim, or with the separate pre-rotation pass, as an exact two-term bf16 split
+ * (hi + lo, three products).  fp16 holds |v| <= 65504: a larger rotated value (or
+ * dim 24..31 value at rotary_dim 24) makes the results invalid and is reported as
+ * NEOX_ERR_DEVICE_RANGE; NEOX_ROTATION_PRE (neox_attn_fwd_ex, rotary_dim 16/24/32)
+ * accepts the whole bf16 range.
+ *
  * Errors: every argument is validated before any CUDA call; on error nothing is
  * launched and nothing is written.  NEOX_ERR_CUDA means a launch or allocation
- * failed.  A device-side wait timeout is reported only by
- * neox_attn_get_device_error() after the stream has been synchronized.
+ * failed.  A device-side wait timeout, and a value beyond the fp16 range (above), is
+ * reported only by neox_attn_get_device_error() after the stream has been synchronized.
  */
 int neox_attn_fwd(const void* qkv, int B, int S, int H, int D, int rotary_dim, float rotary_base,
                   void* out, float* lse, void* stream);
 
 /*
- * Where the rotary embedding of Q and K is computed (the results are bit-identical):
+ * Where the rotary embedding of Q and K is computed (bit-identical results, except that
+ * the in-kernel rotation at rotary_dim 16, 24 and 32 rounds the rotated chunks to fp16
+ * where the pass keeps the hi/lo split; see neox_attn_fwd):
  *   NEOX_ROTATION_FUSED  inside the attention kernel, in shared memory, on every K tile
  *                        each query unit streams (no extra HBM traffic; the K tile of a
  *                        head is rotated once per query unit that reads it);
@@ -272,8 +285,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
 /*
  * Reads and clears the current device's error word written by the kernels' bounded
  * waits and input checks.  Call after synchronizing the streams that ran the kernels.
- * Returns NEOX_OK, NEOX_ERR_DEVICE_TIMEOUT, NEOX_ERR_DEVICE_BAD_POSITION (decode
- * only), or NEOX_ERR_CUDA if the read failed.
+ * Returns NEOX_OK, NEOX_ERR_DEVICE_TIMEOUT, NEOX_ERR_DEVICE_RANGE (forward with in-kernel
+ * rotation at rotary_dim 16, 24 or 32), NEOX_ERR_DEVICE_BAD_POSITION (decode only), or
+ * NEOX_ERR_CUDA if the read failed; a timeout is reported before the others.
  */
 int neox_attn_get_device_error(void);
 

@@ -7,7 +7,11 @@ double from one block to the next, and the odd query rows are scaled by 2^-6, so
 scores stay small and they never rescale (warps whose rows mix both cases).  Every scale
 is a power of two, exact in bf16.  Each test first checks on the host, from the oracle's
 own rotated vectors in fp64, that the inputs do produce such events, then compares every
-row with the oracle at the forward tolerances.
+row with the oracle at the forward tolerances.  Scores here reach ~40, far from the
+unit-normal inputs the tolerances are set for; at rotary_dim 16, 24 and 32 the in-kernel
+rotation rounds the rotated chunks to fp16 (about 2^-12 relative, so an absolute lse
+error that grows with the scores), so those cases run the pre-rotated placement (the
+exact hi/lo split).  The rescale path is the same softmax code in both placements.
 """
 import numpy as np
 import pytest
@@ -85,7 +89,8 @@ def test_lazy_rescale_matches_oracle_on_every_row(B, S, H, D, r):
     import causal_rope_self_neox_b300 as na
     qkv = growing_keys_qkv(B, S, H, D, seed=S + D + r)
     assert_premise(rescale_events(qkv, B, S, H, D, r))
-    out, lse = na.attn_fwd(qkv.cuda(), r)
+    rotation = na.NEOX_ROTATION_PRE if r in (16, 24, 32) else na.NEOX_ROTATION_AUTO
+    out, lse = na.attn_fwd(qkv.cuda(), r, 1e4, rotation=rotation)
     torch.cuda.synchronize()
     na.check_device_error()
     ref_out, ref_lse = oracle.fwd(bf16_bits(qkv), B, S, H, D, r, 1e4)

@@ -9,7 +9,10 @@ about 2^-9 relative per element, which on rows with few keys (row 0's lse is a
 single score) is too much.  The kernel therefore splits each rotated value into
 hi = bf16(y) and lo = bf16(y - hi) and accumulates q_hi.k_hi + q_hi.k_lo +
 q_lo.k_hi (the lo.lo term is ~2^-18 relative and dropped).  This test emulates
-both schemes around the oracle and shows that only the split one fits.
+both schemes around the oracle and shows that only the split one fits.  At rotary_dim 16,
+24 and 32 the in-kernel rotation instead rounds the rotated 16-column chunks (dims 0..15,
+or 0..31) once to fp16, 11 significant bits to bf16's 8, with no lo products; its
+emulation has to fit as well.
 """
 import math
 
@@ -27,6 +30,11 @@ def bf16_round(x):
     u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
     u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def f16_round(x):
+    """fp32 -> fp16 round-to-nearest-even, returned as fp64."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float64)
 
 
 def rotate_f32(x, r, base):
@@ -49,6 +57,11 @@ def emulate(q, k, v, r, base, rows, split):
     S, D = q.shape
     qr, kr = rotate_f32(q, r, base), rotate_f32(k, r, base)
     qh, kh = bf16_round(qr), bf16_round(kr)
+    if split == "f16":  # the first ceil(r/16) 16-column chunks in fp16, the rest exact bf16
+        f = 16 * ((r + 15) // 16)
+        qh, kh = qr.copy(), kr.copy()
+        qh[:, :f], kh[:, :f] = f16_round(qr[:, :f]), f16_round(kr[:, :f])
+        split = False
     if split:
         ql, kl = bf16_round(qr - qh), bf16_round(kr - kh)
     c = math.log2(math.e) / math.sqrt(D)
@@ -101,6 +114,13 @@ CASES = {  # name: (B, S, H, D, r, seed, k_scale, rows_per_head)
 def test_split_scheme_fits_tolerances(name):
     omax, orms, lmax = errors(*CASES[name], split=True)
     assert omax <= OUT_MAX / 2 and orms <= OUT_RMS / 2 and lmax <= LSE_MAX / 10, (omax, orms, lmax)
+
+
+@pytest.mark.parametrize("name", ["tiny", "d96_r24", "d128_r32"])
+def test_fp16_chunk_scheme_fits_tolerances(name):
+    cases = dict(CASES, d128_r32=(1, 512, 1, 128, 32, 11, 1.0, 48))
+    omax, orms, lmax = errors(*cases[name], split="f16")
+    assert omax <= OUT_MAX / 2 and orms <= OUT_RMS / 2 and lmax <= LSE_MAX / 2, (omax, orms, lmax)
 
 
 def test_plain_bf16_rotation_breaks_lse_tolerance():
