@@ -695,9 +695,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 constexpr int kSmemLimit = 227 * 1024;
 
 // Ring depths: the deepest (K, V) pair that fits next to the two query tiles, preferring
-// the per-head-dim defaults.
+// the per-head-dim defaults (at D = 128 a K ring of 3 once there are no side tiles).
 inline void pick_rings(int D, int side_cols, int* nk, int* nv) {
-  const int pref_k = D == 64 ? 4 : D == 96 ? 3 : 2, pref_v = D == 64 ? 4 : 2;
+  const bool side = side_cols > 0;
+  const int pref_k = D == 64 ? 4 : D == 96 ? 3 : (side ? 2 : 3);  // D = 96: (4, 3) measured slower
+  const int pref_v = D == 64 ? 4 : 2;
   const int cand[][2] = {{pref_k, pref_v}, {3, 2}, {2, 2}, {2, 1}, {1, 1}};
   for (const auto& c : cand) {
     if (ws_layout(D, side_cols, c[0], c[1]).total() <= kSmemLimit) {
@@ -712,6 +714,7 @@ inline void pick_rings(int D, int side_cols, int* nk, int* nv) {
 template <int D, int RK, bool PRE, bool ALIBI = false>
 int launch_ws_impl(const CUtensorMap& map, const CUtensorMap& map_rot, AttnParams p, int num_sms, cudaStream_t stream,
                    int* last_err) {
+  if (rot_f16(RK, PRE)) p.side_cols = 0;  // fp16 rotated chunks: no lo side tiles
   pick_rings(D, p.side_cols, &p.nk, &p.nv);
   const WsLayout L = ws_layout(D, p.side_cols, p.nk, p.nv);
   auto kern = attn_fwd_ws_kernel<D, RK, PRE, ALIBI>;
