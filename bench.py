@@ -96,14 +96,40 @@ DEC_KERNEL_SOURCES = ("decode.cuh", "attn_common.cuh", "ptx.cuh", "tile_layout.c
 BWD_KERNEL_SOURCES = ("attn_bwd.cuh", "attn_common.cuh", "ptx.cuh", "tile_layout.cuh", "neox_attn.cu")
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with its comments and blank lines removed and trailing whitespace
+    trimmed (string and character literals kept as they are), so that a comment edit
+    leaves the hash of the compiled code unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            while i < n and text[i] != "\n":
+                i += 1
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (l.rstrip() for l in "".join(out).split("\n"))
+    return "\n".join(l for l in lines if l)
+
+
 def kernel_source_hash(sources=FWD_KERNEL_SOURCES) -> str:
-    """Hash of the sources a kernel is compiled and launched from (by default the prefill kernel's)."""
+    """Hash of the code (comments excluded) of the sources a kernel is compiled and launched
+    from (by default the prefill kernel's)."""
     h = hashlib.sha256()
-    files = [os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", n) for n in sources]
-    for f in files:
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
-            h.update(fh.read())
+    for name in sources:
+        with open(os.path.join(ROOT, "causal_rope_self_neox_b300", "csrc", name)) as fh:
+            h.update(name.encode())
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

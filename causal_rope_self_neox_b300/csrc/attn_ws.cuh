@@ -8,7 +8,8 @@
 //   warp 0        TMA producer: Q tiles once per unit, then K_j / V_j into rings
 //   warp 1        tcgen05 issuer (one lane) and TMEM owner
 //   warps 2-3     rotary transform: rotate-half of Q (per unit) and of K_j (per block)
-//                 in shared memory, hi in place, lo to the side tiles.  A unit's K_0 is
+//                 in shared memory (rotary_dim 16/24/32: the rotated chunks as fp16 in
+//                 place; otherwise hi in place, lo to the side tiles).  A unit's K_0 is
 //                 loaded and rotated before its query tiles: K_0's ring slot frees a few
 //                 blocks before the previous unit releases the query buffers, so only the
 //                 query load and rotation remain between two units (the producer also

@@ -33,3 +33,12 @@ def test_bench_rejects_too_few_warmup_steps():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
                          text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "warmup" in out.stderr
+
+
+def test_profile_hash_ignores_comments_but_not_code():
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int a = 1;  // one\n/* block\ncomment */\n\nasm("x // y" : "=r"(a));\nchar c = \'"\';\n'
+    assert bench.code_only(src) == 'int a = 1;\nasm("x // y" : "=r"(a));\nchar c = \'"\';'
+    assert bench.code_only(src.replace("// one", "// two")) == bench.code_only(src)
+    assert bench.code_only(src.replace("a = 1", "a = 2")) != bench.code_only(src)
