@@ -57,6 +57,8 @@ def check(got, ref, what):
     (1, 384, 1, 96, 6),      # rotary_dim not a multiple of 8
     (1, 1000, 1, 128, 32),
     (1, 700, 2, 96, 24),     # six key blocks, ragged: both query-side buffers cycle (dq' staged in them)
+    (1, 300, 2, 128, 40),    # two of four 32-column blocks of q', k' rotated, two read from the input
+    (1, 260, 1, 96, 48),     # two of three rotated
 ])
 def test_bwd_small_shapes(B, S, H, D, r):
     qkv = make_qkv(B, S, H, D, seed=S + D + r)
