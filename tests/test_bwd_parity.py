@@ -68,15 +68,46 @@ def test_bwd_small_shapes(B, S, H, D, r):
     check(got, ref, f"{B},{S},{H},{D},{r}")
 
 
-def test_bwd_neox20b_sampled_heads():
-    # the full neox20b-shaped problem on the GPU; heads are independent, so a few
-    # (b, h) slices are checked against the oracle run on those heads alone
-    w = WORKLOADS["neox20b"]
+# (b, h) slices per workload: first and last heads, and both sides of each boundary between
+# the kernel's L2 head groups (48 MB of Q'/dO per group: 64 heads for neox20b, so the
+# groups are the batches; 48 for pythia1.4b, whose 64 heads leave a short second group;
+# one group of all 96 heads for pythia160m)
+SAMPLED_HEADS = {
+    "neox20b": ((0, 0), (0, 37), (0, 63), (1, 0), (1, 63)),
+    "pythia1.4b": ((0, 0), (2, 15), (3, 0), (3, 15)),
+    "pythia160m": ((0, 0), (4, 7), (7, 11)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SAMPLED_HEADS))
+def test_bwd_workload_sampled_heads(name):
+    # the full workload-shaped problem on the GPU, as the benchmark runs it; heads are
+    # independent, so a few (b, h) slices are checked against the oracle run on those
+    # heads alone
+    w = WORKLOADS[name]
     qkv = make_qkv(w.B, w.S, w.H, w.D, w.seed, w.k_scale)
     dout = make_dout(w.B, w.S, w.H, w.D, seed=w.seed)
     got = gpu_bwd(qkv, dout, w.rotary_dim)
-    for b, h in ((0, 0), (0, 37), (1, 63)):
+    for b, h in SAMPLED_HEADS[name]:
         q1 = qkv[b:b + 1, :, h:h + 1].contiguous()
         g1 = dout[b:b + 1, :, h:h + 1].contiguous()
         ref = oracle.bwd(bf16_bits(q1), bf16_bits(g1), 1, w.S, 1, w.D, w.rotary_dim)
-        check(got[b:b + 1, :, h:h + 1], ref, f"neox20b b={b} h={h}")
+        check(got[b:b + 1, :, h:h + 1], ref, f"{name} b={b} h={h}")
+
+
+def test_bwd_repeat_calls_dk_dv_bit_identical_dq_within_one_rounding():
+    # dk and dv accumulate inside one CTA in a fixed order: bit-identical from call to call.
+    # dq' is summed in fp32 by tensor reductions from the CTAs of every key block, in the
+    # order they land, so dq may differ by one bf16 rounding of nearly equal fp32 sums
+    import causal_rope_self_neox_b300 as na
+    B, S, H, D, r = 1, 1100, 3, 96, 24
+    qkv = make_qkv(B, S, H, D, seed=31).cuda()
+    dout = make_dout(B, S, H, D, seed=31).cuda()
+    out, lse = na.attn_fwd(qkv, r)
+    g1 = na.attn_bwd(qkv, out, lse, dout, r)
+    g2 = na.attn_bwd(qkv, out, lse, dout, r)
+    na.check_device_error()
+    assert torch.equal(g1[..., 1:, :], g2[..., 1:, :])
+    a, b = g1[..., 0, :].float(), g2[..., 0, :].float()
+    bound = 2.0 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-5 * a.abs().max()
+    assert bool(((a - b).abs() <= bound).all())
