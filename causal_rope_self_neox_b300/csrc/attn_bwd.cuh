@@ -12,8 +12,10 @@
 // Three kernels on the caller's stream:
 //   attn_bwd_prep_kernel   the rotated q', k' (bf16, rounded once) into a scratch copy of
 //                          qkv, delta_i (fp32) and a zeroed fp32 dq' accumulator;
-//   attn_bwd_kernel        one CTA per (key block j, head): K'_j, V_j stay in shared
-//                          memory while query blocks i >= j stream through; per block
+//   attn_bwd_kernel        persistent, one CTA per SM taking work items (key block j,
+//                          head) in a fixed order from a counter: K'_j, V_j stay in shared
+//                          memory while query blocks i >= j stream through (the next
+//                          item's K'/V, and its first Q'/dO, load under the epilogue); per block
 //                          five tcgen05 MMAs (S = Q'K'^T and dP = dO V^T into TMEM, then
 //                          dV += P^T dO and dK += dS^T Q' accumulating in TMEM over i, and
 //                          dQ'_i = dS K' added to the fp32 accumulator by D/32 TMA tensor
@@ -50,6 +52,10 @@ struct BwdParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Work counter of the main kernel (items past the grid's first), zeroed by the prep kernel
+// of the same call (calls on one device are serialised by the shared scratch anyway).
+__device__ unsigned int g_bwd_next;
+
 // Per row (one warp per row): slots 0, 1 of qkv_rot = R(s) q, R(s) k in bf16 (the
 // rotation rounded once, as the MMAs take it), delta = dout . out (fp32), and dq_acc
 // zeroed.  16-byte loads and stores; the row's q and k wait in shared memory (fp32) so
@@ -59,6 +65,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   constexpr int C8 = D / 8;  // 16-byte chunks per D-vector
   __shared__ float xbuf[8][2 * D];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0 && threadIdx.x == 0) g_bwd_next = 0u;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + w;  // [b][s][h]
   if (row >= static_cast<long long>(p.B) * p.S * p.H) return;
   const long long s = (row / p.H) % p.S;
@@ -225,20 +232,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  int* next_slot = reinterpret_cast<int*>(tmem_slot + 2);  // the CTA's next work item
+
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & (kRows - 1), part = tid >> 7;  // tile row, quarter of the row
-  // CTA order: heads in groups of heads_per_group (their Q'/dO tiles, read by every key
-  // block of a head, stay in L2 while the group runs); inside a group the heaviest key
-  // blocks (j = 0, every query block) come first
+  // Work items (key block j, head), taken in order: heads in groups of heads_per_group
+  // (their Q'/dO tiles, read by every key block of a head, stay in L2 while the group
+  // runs); inside a group the heaviest key blocks (j = 0, every query block) come first.
+  // A CTA's first item is its block index, every later one comes from the work counter.
   const int BH = p.B * p.H;
-  const int per_group = p.heads_per_group * p.nblk;
-  const int grp_id = blockIdx.x / per_group;
-  const int g0 = grp_id * p.heads_per_group;
-  const int gh = min(p.heads_per_group, BH - g0);  // heads in this group (the last may be short)
-  const int rem = blockIdx.x - grp_id * per_group;
-  const int j = rem / gh;
-  const int bh = g0 + (rem - j * gh);
-  const int b = bh / p.H, h = bh - b * p.H;
+  const int total = p.nblk * BH;
+  auto item_jbh = [&](int it, int& jj, int& bb, int& hh) {
+    const int per_group = p.heads_per_group * p.nblk;
+    const int grp_id = it / per_group;
+    const int g0 = grp_id * p.heads_per_group;
+    const int gh = min(p.heads_per_group, BH - g0);  // heads in this group (the last may be short)
+    const int rem = it - grp_id * per_group;
+    jj = rem / gh;
+    const int bh = g0 + (rem - jj * gh);
+    bb = bh / p.H;
+    hh = bh - bb * p.H;
+  };
+  int item = blockIdx.x;
+  int j, b, h;
+  item_jbh(item, j, b, h);
   const uint32_t bar_kv = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[3]), bar_rel = smem_u32(&bars[4]);
   auto bar_ld = [&](int k) { return smem_u32(&bars[1 + k]); };
   const uint64_t lim = p.wait_limit_ns;
@@ -273,14 +290,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // thread 0 only: copies and MMAs in flight, for the abort path
   bool kv_pending = false, mma_pending = false;
   bool ld_pending[2] = {false, false};
-  uint32_t ph_ld[2] = {0, 0}, ph_mma = 0, ph_rel = 0;
-  auto issue_qg = [&](int k, int blk) {  // Q_blk (raw) and dO_blk into buffer k
+  uint32_t ph_kv = 0, ph_ld[2] = {0, 0}, ph_mma = 0, ph_rel = 0;
+  auto issue_qg_of = [&](int k, int blk, int bb, int hh) {  // Q'_blk and dO_blk of head (bb, hh) into buffer k
     mbar_arrive_expect_tx(bar_ld(k), 2 * TB);
     for (int cb = 0; cb < D / kBlkCols; ++cb) {
-      tma_load_4d(smem_u32(Qb(k) + cb * kBlkBytes), &tq, bar_ld(k), cb * kBlkCols, 3 * h + 0, blk * kRows, b);
-      tma_load_4d(smem_u32(Gb(k) + cb * kBlkBytes), &tg, bar_ld(k), cb * kBlkCols, h, blk * kRows, b);
+      tma_load_4d(smem_u32(Qb(k) + cb * kBlkBytes), &tq, bar_ld(k), cb * kBlkCols, 3 * hh + 0, blk * kRows, bb);
+      tma_load_4d(smem_u32(Gb(k) + cb * kBlkBytes), &tg, bar_ld(k), cb * kBlkCols, hh, blk * kRows, bb);
     }
     ld_pending[k] = true;
+  };
+  auto issue_qg = [&](int k, int blk) { issue_qg_of(k, blk, b, h); };
+  auto issue_kv = [&](int jj, int bb, int hh) {  // K'_jj and V_jj of head (bb, hh)
+    mbar_arrive_expect_tx(bar_kv, 2 * TB);
+    for (int cb = 0; cb < D / kBlkCols; ++cb) {
+      tma_load_4d(smem_u32(Kt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * hh + 1, jj * kRows, bb);
+      tma_load_4d(smem_u32(Vt + cb * kBlkBytes), &tv, bar_kv, cb * kBlkCols, 3 * hh + 2, jj * kRows, bb);
+    }
+    kv_pending = true;
   };
   // wait for buffer k's tiles (the query rows arrive rotated)
   auto land = [&](int k, unsigned int site) -> bool {
@@ -294,27 +320,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   bool ok = true;
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_kv, 2 * TB);
-    for (int cb = 0; cb < D / kBlkCols; ++cb) {
-      tma_load_4d(smem_u32(Kt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * h + 1, j * kRows, b);
-      tma_load_4d(smem_u32(Vt + cb * kBlkBytes), &tv, bar_kv, cb * kBlkCols, 3 * h + 2, j * kRows, b);
-    }
-    kv_pending = true;
+    issue_kv(j, b, h);
     issue_qg(0, j);
     if (NB == 2 && j + 1 < p.nblk) issue_qg(1, j + 1);
   }
-  wait_phase(bar_kv, 0, abort_flag, lim, 42);
+  // ---- one work item per pass; the next item's K'/V (and, with two query-side buffers,
+  //      its first Q'/dO tiles) load under this item's epilogue
+  for (;;) {
+  wait_phase(bar_kv, ph_kv, abort_flag, lim, 42);
   __syncthreads();
   const long long key = static_cast<long long>(j) * kRows + row;
   if (*abort_flag) {
     ok = false;
   } else {
+    ph_kv ^= 1;
     if (tid == 0) kv_pending = false;
     ok = land(0, 43);
   }
   fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
+  if (!ok) break;
 
   for (int i = j; i < p.nblk && ok; ++i) {
     const int bi = NB == 2 ? ((i - j) & 1) : 0;
@@ -460,6 +486,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
   }
 
+  if (!ok) break;
+  // ---- the next work item, taken now: its K'/V go into tiles that this item's last MMAs
+  //      have finished reading, and load while the epilogue below runs
+  if (tid == 0) {
+    const int nxt = static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(&g_bwd_next, 1u));
+    *next_slot = nxt;
+    if (nxt < total) {
+      int jn, bn, hn;
+      item_jbh(nxt, jn, bn, hn);
+      issue_kv(jn, bn, hn);
+    }
+  }
+
   // ---- dk = R(key)^T dk' and dv for the rows of key block j, bf16 into slots 1 and 2.
   // dk' is staged in shared memory (padded rows, so the rotation can read the pair partners
   // held by the row's other threads): with two query-side buffers in the P/dS tiles (the
@@ -469,7 +508,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bulk_wait_read_all();
     __syncthreads();
   }
-  if (ok && !*abort_flag) {
+  if (!*abort_flag) {
     tc_fence_after_sync();
     const bool kvalid = key < p.S;
     const int h2 = p.r >> 1;
@@ -504,6 +543,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
       }
     }
+    // two buffers: both free once the last reductions have read their staging; the next
+    // item's first Q'/dO tiles load under the dk rotation
+    if (NB == 2 && tid == 0) {
+      bulk_wait_read_all();
+      const int nxt = *next_slot;
+      if (nxt < total) {
+        int jn, bn, hn;
+        item_jbh(nxt, jn, bn, hn);
+        issue_qg_of(0, jn, bn, hn);
+        if (jn + 1 < p.nblk) issue_qg_of(1, jn + 1, bn, hn);
+      }
+    }
     __syncthreads();
     if (kvalid) {
       for (int d0 = 8 * part; d0 < D; d0 += 32) {
@@ -527,11 +578,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   }
+  // ---- this item's TMEM and staging reads done: hand over to the next item (one buffer:
+  //      its first Q'/dO tiles go into the query-side tiles the dk' staging used)
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    ok = false;
+    break;
+  }
+  item = *next_slot;
+  if (item >= total) break;
+  item_jbh(item, j, b, h);
+  if (NB == 1 && tid == 0) issue_qg(0, j);
+  }  // work items
 
   // ---- teardown: let the copies, reductions and MMAs in flight land, then free TMEM
   bulk_wait_all();
   if (tid == 0) {
-    if (kv_pending) drain_phase(bar_kv, 0, lim);
+    if (kv_pending) drain_phase(bar_kv, ph_kv, lim);
     for (int k = 0; k < 2; ++k)
       if (ld_pending[k]) drain_phase(bar_ld(k), ph_ld[k], lim);
     if (mma_pending) drain_phase(bar_mma, ph_mma, lim);

@@ -499,7 +499,7 @@ int encode_dq_map(CUtensorMap* map, const float* ptr, int B, int S, int H, int D
 
 template <int D>
 int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tg,
-               const CUtensorMap& tdq, cudaStream_t stream) {
+               const CUtensorMap& tdq, int num_sms, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.S * p.H;
   neox::attn_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -507,7 +507,8 @@ int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMa
   const int smem = neox::bwd_smem_bytes(D);
   e = cudaFuncSetAttribute(neox::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  const long long ctas = static_cast<long long>(p.nblk) * p.B * p.H;
+  // persistent: one CTA per SM (at most one per work item), later items from the work counter
+  const long long ctas = std::min<long long>(static_cast<long long>(p.nblk) * p.B * p.H, std::max(num_sms, 1));
   neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tv, tg, tdq, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
@@ -739,9 +740,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
     switch (D) {
-      case 64: return launch_bwd<64>(p, tq, tv, tg, tdq, stream);
-      case 96: return launch_bwd<96>(p, tq, tv, tg, tdq, stream);
-      default: return launch_bwd<128>(p, tq, tv, tg, tdq, stream);
+      case 64: return launch_bwd<64>(p, tq, tv, tg, tdq, dev.num_sms, stream);
+      case 96: return launch_bwd<96>(p, tq, tv, tg, tdq, dev.num_sms, stream);
+      default: return launch_bwd<128>(p, tq, tv, tg, tdq, dev.num_sms, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
