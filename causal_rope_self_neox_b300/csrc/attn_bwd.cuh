@@ -44,7 +44,7 @@ struct BwdParams {
   float* delta;          // fp32 [B, H, S]     scratch
   const float2* cs;      // cos/sin table [>= S rows][r/2]
   int B, S, H, r, nblk;
-  int heads_per_group;   // CTA order: groups of heads whose Q'/dO tiles fit in L2 together
+  int heads_per_group;   // work-item order: groups of heads whose Q'/dO tiles fit in L2 together
   float scale_log2;      // log2(e) / sqrt(D)
   float scale;           // 1 / sqrt(D)
   uint64_t wait_limit_ns;

@@ -277,7 +277,11 @@ int neox_attn_decode(const void* qkv_new, void* k_cache, void* v_cache, const in
  * library's per-device scratch (shared with neox_attn_decode, grown on demand, freed by
  * neox_attn_release) holds an fp32 dq' accumulator of B*S*H*D floats, B*H*S floats of
  * dout.out, and a bf16 copy of qkv's shape holding the rotated q', k' (about 10 bytes
- * per element of out in all), so backward and decode calls must not overlap on the GPU.
+ * per element of out in all), so backward and decode calls must not overlap on the GPU;
+ * two backward calls must not overlap either (they also share the device's work counter
+ * of the main kernel, which is persistent: one CTA per SM).  dk and dv are identical from
+ * call to call; dq can differ by one bf16 rounding, since its fp32 sums are added in the
+ * order the key blocks' partial results arrive.
  */
 int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void* dout, int B, int S, int H, int D,
                   int rotary_dim, float rotary_base, void* dqkv, void* stream);
