@@ -52,6 +52,12 @@ struct BwdParams {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Programmatic dependent launch between the three kernels of a call: a kernel lets the next
+// one launch early (its CTAs set up while this grid drains), and the next one waits for
+// this grid's completion and memory before it reads anything this grid wrote.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prior() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Work counter of the main kernel (items past the grid's first), zeroed by the prep kernel
 // of the same call (calls on one device are serialised by the shared scratch anyway).
 __device__ unsigned int g_bwd_next;
@@ -65,6 +71,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
   constexpr int C8 = D / 8;  // 16-byte chunks per D-vector
   __shared__ float xbuf[8][2 * D];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) g_bwd_next = 0u;
   const long long row = static_cast<long long>(blockIdx.x) * 8 + w;  // [b][s][h]
   if (row >= static_cast<long long>(p.B) * p.S * p.H) return;
@@ -131,6 +138,7 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const BwdParams p) {
 // l handles dims l, l + 32, ...
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_dq_kernel(const BwdParams p) {
+  pdl_wait_prior();  // the main kernel's dq' reductions
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // [b][s][h]
   const int lane = threadIdx.x & 31;
   if (row >= static_cast<long long>(p.B) * p.S * p.H) return;
@@ -277,10 +285,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
+  pdl_launch_dependents();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
+  pdl_wait_prior();  // the prep kernel's q', k', delta, zeroed dq' and work counter
   const uint32_t tS = tbase, tdP = tbase + 128, tdV = tbase + 256, tdK = tbase + 256 + D, tdQ = tbase;
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   constexpr uint32_t idesc_s = idesc_bwd(128, 128, false, false);  // S, dP

@@ -507,12 +507,26 @@ int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMa
   const int smem = neox::bwd_smem_bytes(D);
   e = cudaFuncSetAttribute(neox::attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  // persistent: one CTA per SM (at most one per work item), later items from the work counter
+  // persistent: one CTA per SM (at most one per work item), later items from the work counter.
+  // The main and dq kernels are launched as programmatic dependents of the kernel before
+  // them (each waits in-kernel for that grid's completion before reading its results).
   const long long ctas = std::min<long long>(static_cast<long long>(p.nblk) * p.B * p.H, std::max(num_sms, 1));
-  neox::attn_bwd_kernel<D><<<static_cast<unsigned>(ctas), neox::kBwdThreads, smem, stream>>>(tq, tv, tg, tdq, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  neox::attn_bwd_dq_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
-  e = cudaGetLastError();
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(neox::kBwdThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, neox::attn_bwd_kernel<D>, tq, tv, tg, tdq, p);
+  if (e != cudaSuccess) return cuda_fail(e);
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, neox::attn_bwd_dq_kernel<D>, p);
   return e == cudaSuccess ? NEOX_OK : cuda_fail(e);
 }
 
