@@ -59,6 +59,11 @@ def check(got, ref, what):
     (1, 700, 2, 96, 24),     # six key blocks, ragged: both query-side buffers cycle (dq' staged in them)
     (1, 300, 2, 128, 40),    # two of four 32-column blocks of q', k' rotated, two read from the input
     (1, 260, 1, 96, 48),     # two of three rotated
+    # 150 (key block, head) work items, two more than a 148-SM GPU has CTAs: the first
+    # items come from the grid, the rest from the work counter (two query-side buffers,
+    # and one at D = 128)
+    (1, 1280, 15, 64, 16),
+    (1, 1280, 15, 128, 32),
 ])
 def test_bwd_small_shapes(B, S, H, D, r):
     qkv = make_qkv(B, S, H, D, seed=S + D + r)
