@@ -241,6 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   int* next_slot = reinterpret_cast<int*>(tmem_slot + 2);  // the CTA's next work item
+  volatile int* kv_pending = reinterpret_cast<volatile int*>(tmem_slot + 3);  // K'/V copies in flight
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & (kRows - 1), part = tid >> 7;  // tile row, quarter of the row
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_mma, 1);
     mbar_init(bar_rel, 1);
     *abort_flag = 0;
+    *kv_pending = 0;
     fence_barrier_init();
     tma_prefetch_map(&tq);
     tma_prefetch_map(&tg);
@@ -297,8 +299,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr uint32_t idesc_t = idesc_bwd(128, D, true, true);      // dV, dK: A = P^T / dS^T
   constexpr uint32_t idesc_q = idesc_bwd(128, D, false, true);     // dQ: A = dS, B = K'
 
-  // thread 0 only: copies and MMAs in flight, for the abort path
-  bool kv_pending = false, mma_pending = false;
+  // thread 0 only: copies and MMAs in flight, for the abort path (the K'/V flag lives in
+  // shared memory: an epilogue's K'/V copies may be issued by another thread)
+  bool mma_pending = false;
   bool ld_pending[2] = {false, false};
   uint32_t ph_kv = 0, ph_ld[2] = {0, 0}, ph_mma = 0, ph_rel = 0;
   auto issue_qg_of = [&](int k, int blk, int bb, int hh) {  // Q'_blk and dO_blk of head (bb, hh) into buffer k
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_load_4d(smem_u32(Kt + cb * kBlkBytes), &tq, bar_kv, cb * kBlkCols, 3 * hh + 1, jj * kRows, bb);
       tma_load_4d(smem_u32(Vt + cb * kBlkBytes), &tv, bar_kv, cb * kBlkCols, 3 * hh + 2, jj * kRows, bb);
     }
-    kv_pending = true;
+    *kv_pending = 1;
   };
   // wait for buffer k's tiles (the query rows arrive rotated)
   auto land = [&](int k, unsigned int site) -> bool {
@@ -344,7 +347,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ok = false;
   } else {
     ph_kv ^= 1;
-    if (tid == 0) kv_pending = false;
+    if (tid == 0) *kv_pending = 0;
     ok = land(0, 43);
   }
   fence_proxy_async_smem();
@@ -498,8 +501,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (!ok) break;
   // ---- the next work item, taken now: its K'/V go into tiles that this item's last MMAs
-  //      have finished reading, and load while the epilogue below runs
-  if (tid == 0) {
+  //      have finished reading, and load while the epilogue below runs.  The counter's round
+  //      trip is taken by a thread with the least staging below (row 0 of the last quarter:
+  //      one 16-column chunk of dk' and of dv where D < 128), so that it does not hold up
+  //      the barrier after the staging
+  if (tid == (D < 128 ? 3 * kRows : 0)) {
     const int nxt = static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(&g_bwd_next, 1u));
     *next_slot = nxt;
     if (nxt < total) {
@@ -553,10 +559,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                          pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
       }
     }
-    // two buffers: both free once the last reductions have read their staging; the next
-    // item's first Q'/dO tiles load under the dk rotation
+    // two buffers: both free once the last reductions have read their staging (thread 0's
+    // bulk groups); the next item's first Q'/dO tiles load under the dk rotation
+    if (NB == 2 && tid == 0) bulk_wait_read_all();
+    __syncthreads();
     if (NB == 2 && tid == 0) {
-      bulk_wait_read_all();
       const int nxt = *next_slot;
       if (nxt < total) {
         int jn, bn, hn;
@@ -565,7 +572,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (jn + 1 < p.nblk) issue_qg_of(1, jn + 1, bn, hn);
       }
     }
-    __syncthreads();
     if (kvalid) {
       for (int d0 = 8 * part; d0 < D; d0 += 32) {
         const bool first = d0 == 8 * part;
@@ -605,7 +611,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // ---- teardown: let the copies, reductions and MMAs in flight land, then free TMEM
   bulk_wait_all();
   if (tid == 0) {
-    if (kv_pending) drain_phase(bar_kv, ph_kv, lim);
+    if (*kv_pending) drain_phase(bar_kv, ph_kv, lim);
     for (int k = 0; k < 2; ++k)
       if (ld_pending[k]) drain_phase(bar_ld(k), ph_ld[k], lim);
     if (mma_pending) drain_phase(bar_mma, ph_mma, lim);
