@@ -217,6 +217,14 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* map, uint32_t ssrc
                "r"(ssrc), "r"(c0), "r"(c1), "r"(c2)
                : "memory");
 }
+// Tensor store of a tile from shared memory (4-D map, coordinates innermost first), tracked
+// in this thread's bulk async-group; rows past the tensor's extent are skipped.
+__device__ __forceinline__ void tma_store_4d(const void* map, uint32_t ssrc, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(ssrc), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -224,7 +232,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
                     const __grid_constant__ CUtensorMap tg, const __grid_constant__ CUtensorMap tdq,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tdo, const BwdParams p) {
   constexpr int NB = bwd_qbufs(D);
   constexpr int TB = tile_bytes(D);
   extern __shared__ uint8_t smem_raw[];
@@ -282,6 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_map(&tg);
     tma_prefetch_map(&tv);
     tma_prefetch_map(&tdq);
+    tma_prefetch_map(&tdo);
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -350,6 +359,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (tid == 0) *kv_pending = 0;
     ok = land(0, 43);
   }
+  // the previous item's dk/dv tensor stores have read their tiles before P/dS overwrites them
+  if (tid == 0) bulk_wait_read_all();
   fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
@@ -528,7 +539,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after_sync();
     const bool kvalid = key < p.S;
     const int h2 = p.r >> 1;
-    uint16_t* dst = p.dqkv + ((static_cast<long long>(b) * p.S + (kvalid ? key : 0)) * p.H + h) * 3 * D;
     // the table entries of this thread's first 8-dim group, requested before the staging
     float2 cs0[8];
 #pragma unroll
@@ -544,21 +554,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int k = 0; k < 16; ++k) xs[c0 + k] = __uint_as_float(r[k]);
     }
-    // dv needs no partner: written while the other threads finish staging dk'
-    for (int c0 = 16 * part; c0 < D; c0 += 64) {
-      uint32_t r[16];
-      tmem_ld16(tdV + lane_off + c0, r);
-      tmem_wait_ld();
-      if (kvalid) {
-#pragma unroll
-        for (int k = 0; k < 16; k += 8)
-          *reinterpret_cast<uint4*>(dst + 2 * D + c0 + k) =
-              make_uint4(pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
-                         pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
-                         pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
-                         pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
-      }
-    }
     // two buffers: both free once the last reductions have read their staging (thread 0's
     // bulk groups); the next item's first Q'/dO tiles load under the dk rotation
     if (NB == 2 && tid == 0) bulk_wait_read_all();
@@ -572,26 +567,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (jn + 1 < p.nblk) issue_qg_of(1, jn + 1, bn, hn);
       }
     }
-    if (kvalid) {
-      for (int d0 = 8 * part; d0 < D; d0 += 32) {
-        const bool first = d0 == 8 * part;
-        float y[8];
+    // dk = R(key)^T dk' for this thread's D/32 groups of 8 dims, into registers (rows past S
+    // are zeros: the tensor stores below skip them)
+    uint32_t dkp[D / 32][4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int d = d0 + e;
-          float v = xs[d];
-          if (d < h2) {
-            const float2 c = first ? cs0[e] : p.cs[key * h2 + d];
-            v = fmaf(v, c.x, xs[d + h2] * c.y);
-          } else if (d < p.r) {
-            const float2 c = first ? cs0[e] : p.cs[key * h2 + (d - h2)];
-            v = fmaf(v, c.x, -xs[d - h2] * c.y);
-          }
-          y[e] = v;
+    for (int g = 0; g < D / 32; ++g) {
+      const int d0 = 8 * part + 32 * g;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int d = d0 + e;
+        float v = kvalid ? xs[d] : 0.0f;
+        if (kvalid && d < h2) {
+          const float2 c = g == 0 ? cs0[e] : p.cs[key * h2 + d];
+          v = fmaf(v, c.x, xs[d + h2] * c.y);
+        } else if (kvalid && d < p.r) {
+          const float2 c = g == 0 ? cs0[e] : p.cs[key * h2 + (d - h2)];
+          v = fmaf(v, c.x, -xs[d - h2] * c.y);
         }
-        *reinterpret_cast<uint4*>(dst + D + d0) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                             pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+        y[e] = v;
       }
+      dkp[g][0] = pack_bf16x2(y[0], y[1]);
+      dkp[g][1] = pack_bf16x2(y[2], y[3]);
+      dkp[g][2] = pack_bf16x2(y[4], y[5]);
+      dkp[g][3] = pack_bf16x2(y[6], y[7]);
+    }
+    __syncthreads();  // every row's dk' has been read: the staging area is free
+    // dk and dv as bf16 tiles in the loads' 64-byte-swizzled layout, in the P/dS tiles (free:
+    // this item's MMAs are done, and with one buffer its last reduction has read them)
+    uint8_t* const tk = Pt;
+    uint8_t* const tvo = Pt + TB;
+#pragma unroll
+    for (int g = 0; g < D / 32; ++g)
+      *reinterpret_cast<uint4*>(tk + sw64_off(row, 8 * part + 32 * g)) =
+          make_uint4(dkp[g][0], dkp[g][1], dkp[g][2], dkp[g][3]);
+    for (int c0 = 16 * part; c0 < D; c0 += 64) {
+      uint32_t r[16];
+      tmem_ld16(tdV + lane_off + c0, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 16; k += 8)
+        *reinterpret_cast<uint4*>(tvo + sw64_off(row, c0 + k)) =
+            make_uint4(pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                       pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                       pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
+                       pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    // slots 1 and 2 of the key block's rows by tensor stores (the next item waits for them
+    // to have read the tiles before its first P/dS)
+    if (tid == 0) {
+      for (int cb = 0; cb < D / kBlkCols; ++cb) {
+        tma_store_4d(&tdo, smem_u32(tk + cb * kBlkBytes), cb * kBlkCols, 3 * h + 1, j * kRows, b);
+        tma_store_4d(&tdo, smem_u32(tvo + cb * kBlkBytes), cb * kBlkCols, 3 * h + 2, j * kRows, b);
+      }
+      bulk_commit_group();
     }
   }
   // ---- this item's TMEM and staging reads done: hand over to the next item (one buffer:

@@ -499,7 +499,7 @@ int encode_dq_map(CUtensorMap* map, const float* ptr, int B, int S, int H, int D
 
 template <int D>
 int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tg,
-               const CUtensorMap& tdq, int num_sms, cudaStream_t stream) {
+               const CUtensorMap& tdq, const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
   const long long rows = static_cast<long long>(p.B) * p.S * p.H;
   neox::attn_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
@@ -521,7 +521,7 @@ int launch_bwd(const neox::BwdParams& p, const CUtensorMap& tq, const CUtensorMa
   cfg.stream = stream;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, neox::attn_bwd_kernel<D>, tq, tv, tg, tdq, p);
+  e = cudaLaunchKernelEx(&cfg, neox::attn_bwd_kernel<D>, tq, tv, tg, tdq, tdo, p);
   if (e != cudaSuccess) return cuda_fail(e);
   cfg.gridDim = dim3(static_cast<unsigned>((rows + 7) / 8));
   cfg.blockDim = dim3(256);
@@ -732,6 +732,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     CUtensorMap tdq;  // the fp32 dq' accumulator at the start of the scratch
     rc = encode_dq_map(&tdq, scratch, B, S, H, D);
     if (rc != NEOX_OK) return rc;
+    CUtensorMap tdo;  // dqkv, for the tensor stores of dk and dv
+    rc = encode_qkv_map(&tdo, dqkv, B, S, H, D);
+    if (rc != NEOX_OK) return rc;
     neox::BwdParams p{};
     p.qkv = static_cast<const uint16_t*>(qkv);
     p.out = static_cast<const uint16_t*>(out);
@@ -754,9 +757,9 @@ int neox_attn_bwd(const void* qkv, const void* out, const float* lse, const void
     p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
     p.wait_limit_ns = neox::kWaitLimitNs;
     switch (D) {
-      case 64: return launch_bwd<64>(p, tq, tv, tg, tdq, dev.num_sms, stream);
-      case 96: return launch_bwd<96>(p, tq, tv, tg, tdq, dev.num_sms, stream);
-      default: return launch_bwd<128>(p, tq, tv, tg, tdq, dev.num_sms, stream);
+      case 64: return launch_bwd<64>(p, tq, tv, tg, tdq, tdo, dev.num_sms, stream);
+      case 96: return launch_bwd<96>(p, tq, tv, tg, tdq, tdo, dev.num_sms, stream);
+      default: return launch_bwd<128>(p, tq, tv, tg, tdq, tdo, dev.num_sms, stream);
     }
   } catch (...) {
     return NEOX_ERR_CUDA;
