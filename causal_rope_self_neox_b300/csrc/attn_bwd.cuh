@@ -22,7 +22,8 @@
 //                          reductions of 128 x 32 boxes, staged, with two query-side
 //                          buffers, in block i's own (then free) Q'/dO buffer and reduced
 //                          while block i+1 computes its P/dS);
-//                          at the end dk (rotated back) and dv are written as bf16;
+//                          at the end dk (rotated back) and dv go out as bf16 tiles by
+//                          TMA tensor stores;
 //   attn_bwd_dq_kernel     rotates the accumulated dq' back and writes dq as bf16.
 // P and dS enter the MMAs as bf16 (fp32 accumulation), as do the rotated q', k' (rounded
 // once, no hi/lo split); the transposed operands P^T, dS^T, dO and Q' are read through
