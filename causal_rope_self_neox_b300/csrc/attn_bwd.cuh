@@ -196,6 +196,15 @@ __host__ __device__ constexpr int bwd_stage_bytes(int D) { return D / 32 * 16384
 __host__ __device__ constexpr int bwd_stage_extra(int D) {
   return bwd_stage_bytes(D) > 2 * tile_bytes(128) ? bwd_stage_bytes(D) - 2 * tile_bytes(128) : 0;
 }
+// Columns of dk' that the epilogue stages in fp32 for the rotation: the 32-column blocks
+// holding rotated dims (the rest goes from TMEM straight into the bf16 dk tile).
+__host__ __device__ constexpr int bwd_rot_cols(int r) { return (r + 31) / 32 * 32; }
+// Where that staging goes: beside the dk and dv tiles in the P/dS area when it fits there,
+// else in the query-side tiles (whose next loads then wait for the end of the epilogue).
+template <int D>
+__host__ __device__ constexpr bool bwd_stage_in_qbuf(int r) {
+  return bwd_qbufs(D) == 1 || bwd_rot_cols(r) * kRows * 4 > 2 * tile_bytes(128) - 2 * tile_bytes(D);
+}
 __host__ __device__ constexpr int bwd_smem_bytes(int D) {
   return 1024 + (2 + 2 * bwd_qbufs(D)) * tile_bytes(D) + 2 * tile_bytes(128) + bwd_stage_extra(D) + 128;
 }
@@ -528,11 +537,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   // ---- dk = R(key)^T dk' and dv for the rows of key block j, bf16 into slots 1 and 2.
-  // dk' is staged in shared memory (padded rows, so the rotation can read the pair partners
-  // held by the row's other threads): with two query-side buffers in the P/dS tiles (the
-  // last block's dq' reduction reads that block's own Q'/dO buffer), with one in the
-  // query-side tiles once that reduction has read them.
-  if (NB == 1) {
+  // staging in the query-side tiles (and, with one buffer, the output tiles over that
+  // block's dq' staging): the last reductions must have read theirs
+  if (bwd_stage_in_qbuf<D>(p.r)) {
     bulk_wait_read_all();
     __syncthreads();
   }
@@ -547,61 +554,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int d = 8 * part + e;
       cs0[e] = kvalid && d < p.r ? p.cs[key * h2 + (d < h2 ? d : d - h2)] : make_float2(1.0f, 0.0f);
     }
-    float* xs = reinterpret_cast<float*>(NB == 2 ? Pt : Qb(0)) + row * (D + 1);
+    // dk and dv leave as bf16 tiles (the loads' 64-byte-swizzled layout) from the P/dS tiles,
+    // free now (this item's MMAs are done; with one buffer its last reduction has read them).
+    // Only the 32-column blocks holding rotated dims go through the fp32 staging, where the
+    // rotation finds the pair partners held by the row's other threads.
+    uint8_t* const tk = Pt;
+    uint8_t* const tvo = Pt + TB;
+    const int rc = bwd_rot_cols(p.r);
+    float* xs = bwd_stage_in_qbuf<D>(p.r) ? reinterpret_cast<float*>(Qb(0)) + row * rc
+                                          : reinterpret_cast<float*>(Pt + 2 * TB) + row * rc;
+    auto xcol = [&](int c) { return c ^ (row & 31); };  // a warp's 32 rows on one column: 32 banks
     for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
       tmem_ld16(tdK + lane_off + c0, r);
       tmem_wait_ld();
+      if (c0 < rc) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) xs[c0 + k] = __uint_as_float(r[k]);
-    }
-    // two buffers: both free once the last reductions have read their staging (thread 0's
-    // bulk groups); the next item's first Q'/dO tiles load under the dk rotation
-    if (NB == 2 && tid == 0) bulk_wait_read_all();
-    __syncthreads();
-    if (NB == 2 && tid == 0) {
-      const int nxt = *next_slot;
-      if (nxt < total) {
-        int jn, bn, hn;
-        item_jbh(nxt, jn, bn, hn);
-        issue_qg_of(0, jn, bn, hn);
-        if (jn + 1 < p.nblk) issue_qg_of(1, jn + 1, bn, hn);
+        for (int k = 0; k < 16; ++k) xs[xcol(c0 + k)] = __uint_as_float(r[k]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; k += 8)
+          *reinterpret_cast<uint4*>(tk + sw64_off(row, c0 + k)) =
+              make_uint4(pack_bf16x2(__uint_as_float(r[k]), __uint_as_float(r[k + 1])),
+                         pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
+                         pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
+                         pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
       }
     }
-    // dk = R(key)^T dk' for this thread's D/32 groups of 8 dims, into registers (rows past S
-    // are zeros: the tensor stores below skip them)
-    uint32_t dkp[D / 32][4];
-#pragma unroll
-    for (int g = 0; g < D / 32; ++g) {
-      const int d0 = 8 * part + 32 * g;
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int d = d0 + e;
-        float v = kvalid ? xs[d] : 0.0f;
-        if (kvalid && d < h2) {
-          const float2 c = g == 0 ? cs0[e] : p.cs[key * h2 + d];
-          v = fmaf(v, c.x, xs[d + h2] * c.y);
-        } else if (kvalid && d < p.r) {
-          const float2 c = g == 0 ? cs0[e] : p.cs[key * h2 + (d - h2)];
-          v = fmaf(v, c.x, -xs[d - h2] * c.y);
-        }
-        y[e] = v;
-      }
-      dkp[g][0] = pack_bf16x2(y[0], y[1]);
-      dkp[g][1] = pack_bf16x2(y[2], y[3]);
-      dkp[g][2] = pack_bf16x2(y[4], y[5]);
-      dkp[g][3] = pack_bf16x2(y[6], y[7]);
-    }
-    __syncthreads();  // every row's dk' has been read: the staging area is free
-    // dk and dv as bf16 tiles in the loads' 64-byte-swizzled layout, in the P/dS tiles (free:
-    // this item's MMAs are done, and with one buffer its last reduction has read them)
-    uint8_t* const tk = Pt;
-    uint8_t* const tvo = Pt + TB;
-#pragma unroll
-    for (int g = 0; g < D / 32; ++g)
-      *reinterpret_cast<uint4*>(tk + sw64_off(row, 8 * part + 32 * g)) =
-          make_uint4(dkp[g][0], dkp[g][1], dkp[g][2], dkp[g][3]);
     for (int c0 = 16 * part; c0 < D; c0 += 64) {
       uint32_t r[16];
       tmem_ld16(tdV + lane_off + c0, r);
@@ -613,6 +592,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        pack_bf16x2(__uint_as_float(r[k + 2]), __uint_as_float(r[k + 3])),
                        pack_bf16x2(__uint_as_float(r[k + 4]), __uint_as_float(r[k + 5])),
                        pack_bf16x2(__uint_as_float(r[k + 6]), __uint_as_float(r[k + 7])));
+    }
+    // two buffers with the staging beside the output tiles: both buffers are free once the
+    // last reductions have read their staging (thread 0's bulk groups); the next item's first
+    // Q'/dO tiles load under the rotation
+    const bool early_qg = NB == 2 && !bwd_stage_in_qbuf<D>(p.r);
+    if (early_qg && tid == 0) bulk_wait_read_all();
+    __syncthreads();
+    if (early_qg && tid == 0) {
+      const int nxt = *next_slot;
+      if (nxt < total) {
+        int jn, bn, hn;
+        item_jbh(nxt, jn, bn, hn);
+        issue_qg_of(0, jn, bn, hn);
+        if (jn + 1 < p.nblk) issue_qg_of(1, jn + 1, bn, hn);
+      }
+    }
+    // dk = R(key)^T dk' on the staged columns, this thread's 8-dim groups (rows past S are
+    // zeros: the tensor stores skip them)
+    for (int d0 = 8 * part; d0 < rc; d0 += 32) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int d = d0 + e;
+        float v = kvalid ? xs[xcol(d)] : 0.0f;
+        if (kvalid && d < h2) {
+          const float2 c = d0 == 8 * part ? cs0[e] : p.cs[key * h2 + d];
+          v = fmaf(v, c.x, xs[xcol(d + h2)] * c.y);
+        } else if (kvalid && d < p.r) {
+          const float2 c = d0 == 8 * part ? cs0[e] : p.cs[key * h2 + (d - h2)];
+          v = fmaf(v, c.x, -xs[xcol(d - h2)] * c.y);
+        }
+        y[e] = v;
+      }
+      *reinterpret_cast<uint4*>(tk + sw64_off(row, d0)) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                                     pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -637,7 +651,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   item = *next_slot;
   if (item >= total) break;
   item_jbh(item, j, b, h);
-  if (NB == 1 && tid == 0) issue_qg(0, j);
+  if (bwd_stage_in_qbuf<D>(p.r) && tid == 0) {  // its staging used the query-side tiles
+    issue_qg(0, j);
+    if (NB == 2 && j + 1 < p.nblk) issue_qg(1, j + 1);
+  }
   }  // work items
 
   // ---- teardown: let the copies, reductions and MMAs in flight land, then free TMEM
