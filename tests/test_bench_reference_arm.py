@@ -1,5 +1,6 @@
 """bench.py's reference arm (the fp64 oracle on the host cores) runs without a GPU: its JSON
-line carries the keys the benchmark contract asks for, on the forward and the projection."""
+line carries the keys the benchmark contract asks for, on the forward, the projection and
+the backward."""
 import json
 import os
 import subprocess
@@ -19,7 +20,7 @@ def run_bench(*args):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("extra", [[], ["--pass", "proj"]])
+@pytest.mark.parametrize("extra", [[], ["--pass", "proj"], ["--pass", "bwd"]])
 def test_reference_arm_line(extra):
     d = run_bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3", *extra)
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
