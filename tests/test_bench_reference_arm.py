@@ -43,3 +43,10 @@ def test_profile_hash_ignores_comments_but_not_code():
     assert bench.code_only(src) == 'int a = 1;\nasm("x // y" : "=r"(a));\nchar c = \'"\';'
     assert bench.code_only(src.replace("// one", "// two")) == bench.code_only(src)
     assert bench.code_only(src.replace("a = 1", "a = 2")) != bench.code_only(src)
+
+
+def test_reference_arm_line_for_decode():
+    d = run_bench("--impl", "reference", "--workload", "pythia160m-decode", "--steps", "3", "--warmup", "3")
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0 and d["steps"] == 3
+    assert d["e2e"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle" and d["gpu_launches"] == 0
+    assert d["config"]["workload"] == "pythia160m-decode" and 1 <= d["config"]["sample_sequences_per_step"] <= 64
