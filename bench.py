@@ -240,7 +240,9 @@ def cpu_baseline(w, qkv_cpu):
 
 
 def run_reference(args, w):
-    """The oracle as the reference arm: each step is a bounded sample of whole heads."""
+    """The oracle as the reference arm: each step is a bounded sample of whole heads (with
+    --alibi, of the ALiBi oracle: the same work per head, with the slopes of a model of as
+    many heads as the sample holds)."""
     import oracle
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -249,10 +251,17 @@ def run_reference(args, w):
     qkv = make_qkv(w.B, w.S, w.H, w.D, w.seed, w.k_scale)
     bits_all = bf16_bits(qkv)
     head_flops = 2.0 * w.S * w.S * w.D
+    alibi = bool(getattr(args, "alibi", False))
+
+    def fwd_heads(bits, n, thr):
+        if alibi:
+            return oracle.fwd_alibi(bits, 1, w.S, n, w.D, threads=thr)
+        return oracle.fwd(bits, 1, w.S, n, w.D, w.rotary_dim, w.rotary_base, threads=thr)
+
     # calibrate: one head on one thread
     one = bf16_bits(qkv[:1, :, :1].contiguous())
     t0 = time.perf_counter()
-    oracle.fwd(one, 1, w.S, 1, w.D, w.rotary_dim, w.rotary_base, threads=1)
+    fwd_heads(one, 1, 1)
     per_head_1t = time.perf_counter() - t0
     budget = 120.0
     per_step_budget = budget / max(1, args.steps + args.warmup)
@@ -260,11 +269,12 @@ def run_reference(args, w):
     heads = min(heads, w.H)
     sub = bf16_bits(qkv[:1, :, :heads].contiguous())
     used = min(threads, heads)
-    run = lambda: oracle.fwd(sub, 1, w.S, heads, w.D, w.rotary_dim, w.rotary_base, threads=used)
+    run = lambda: fwd_heads(sub, heads, used)
     flops = heads * head_flops
-    sample = f"{heads} of {w.B * w.H} heads x {w.S} rows per step, fp64"
+    sample = f"{heads} of {w.B * w.H} heads x {w.S} rows per step, fp64" + \
+        (f", ALiBi with the slopes of a {heads}-head model" if alibi else "")
     # a head runs on one thread: a step takes about per_head_1t * ceil(heads / used)
-    if per_head_1t * -(-heads // used) > 1.5 * per_step_budget:
+    if not alibi and per_head_1t * -(-heads // used) > 1.5 * per_step_budget:
         # too long for the budget: evenly spaced query rows of head (0, 0) on all threads,
         # counted at their exact causal cost 4 (i + 1) D, so the whole run stays near it
         one = bf16_bits(qkv[:1, :, :1].contiguous())
@@ -297,7 +307,8 @@ def run_reference(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {**w.describe(), "sample_heads_per_step": heads, "l2": "n/a (CPU)"},
+        "config": {**w.describe(), "sample_heads_per_step": heads, "l2": "n/a (CPU)",
+                   **({"rotation": "none: ALiBi bias -m_h (i - j) instead (the ALiBi oracle)"} if alibi else {})},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -20,7 +20,7 @@ def run_bench(*args):
     return json.loads(lines[0])
 
 
-@pytest.mark.parametrize("extra", [[], ["--pass", "proj"], ["--pass", "bwd"]])
+@pytest.mark.parametrize("extra", [[], ["--pass", "proj"], ["--pass", "bwd"], ["--alibi"]])
 def test_reference_arm_line(extra):
     d = run_bench("--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3", *extra)
     assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 3 and d["warmup"] == 3
